@@ -1,0 +1,353 @@
+#!/usr/bin/env python3
+"""Benchmark: blockwise ring self-attention forward on GB300.
+
+One step = one rsa_ring_attn_fwd call over the whole workload (every block-
+attention pair of every ring round and every merge), inputs resident in HBM.
+Default workload: the page-1 shape (B=8, H=64, T=32768, d=128, N=4 chunks,
+causal, bf16).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, timed on a sample
+
+Multi-GPU (torchrun): every rank runs its own copy of the workload (independent
+batches, no data exchange); value = all ranks' useful FLOPs / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+_ROOT = os.path.dirname(os.path.abspath(__file__))
+if _ROOT not in sys.path:
+    sys.path.insert(0, _ROOT)
+
+METRIC = "ring-attn fwd TFLOP/s (causal-useful) and % BF16 tensor peak; merge HBM GB/s"
+UNIT = "TFLOP/s"
+
+
+def useful_flops(B, H, T, d, causal):
+    pairs = T * (T + 1) // 2 if causal else T * T
+    return 4.0 * B * H * d * pairs
+
+
+def merge_bytes_per_step(w, sched):
+    """Algorithmic merge bytes of one ring: 10d+12 per row per merge, 8d+12 for
+    a chunk's last (finalising) merge (bf16 partials, fp32 accumulator)."""
+    BH = w.B * w.H
+    Tc = w.T // w.N
+    esz = 2 if w.dtype == "bf16" else 4
+    total = 0
+    for r in range(1, w.N):
+        for (i, j) in sched(r):
+            last = (i if w.causal else w.N - 1) == r
+            if last:
+                per = 4 * w.d + esz * w.d + esz * w.d + 12
+            else:
+                per = 4 * w.d + esz * w.d + 4 * w.d + 12
+            total += BH * Tc * per
+    return total
+
+
+def read_peaks():
+    path = os.path.join(_ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        sm_sorted = sorted(sm)
+        return {"sm_mhz": sm_sorted[len(sm_sorted) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_baseline(w, q_cpu_rows, k_cpu, v_cpu, rows, budget_s=15.0):
+    """Time the oracle (as it stands) on a bounded sample of query rows."""
+    import numpy as np
+    import oracle
+    n_thr = oracle.max_threads()
+    # size the sample: time a small probe, then scale to ~budget_s
+    n_probe = min(16, len(rows))
+    t0 = time.perf_counter()
+    oracle.attend_rows(q_cpu_rows[:n_probe], k_cpu, v_cpu, rows[:n_probe], w.causal)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(min(len(rows), max(n_probe, n_probe * budget_s / dt)))
+    n = max(n_thr, (n // n_thr) * n_thr) if n >= n_thr else n
+    n = min(n, len(rows))
+    t0 = time.perf_counter()
+    oracle.attend_rows(q_cpu_rows[:n], k_cpu, v_cpu, rows[:n], w.causal)
+    dt = time.perf_counter() - t0
+    fl = oracle.rows_flops(rows[:n], w.T, w.d, w.causal)
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": n_thr, "kind": "oracle",
+            "sample": f"{n} sampled query rows of {w.name} (fp64 C, OpenMP over rows), {dt:.1f} s"}
+
+
+def run_reference(args, w):
+    """--impl reference: the CPU oracle on a bounded sample per step."""
+    import numpy as np
+    import torch
+    import oracle
+    import rsa_inputs
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    # inputs drawn on the CPU for the sampled heads only: every head is an
+    # independent problem, so sample rows from one (b, h) slice
+    B1 = rsa_inputs.Workload(w.name, 1, 1, w.T, w.d, w.N, w.causal, w.dtype, w.recipe, w.check)
+    q, k, v = rsa_inputs.make_workload(B1, seed=0, device="cpu")
+    rows = rsa_inputs.sample_rows(B1, n=4096, seed=1)
+    qa = q.view(torch.int16).numpy().view(np.uint16) if q.dtype == torch.bfloat16 else q.numpy()
+    q_rows = np.ascontiguousarray(qa[rows[:, 0], rows[:, 1], rows[:, 2]])
+    n_thr = oracle.max_threads()
+    # rows per step sized so one step takes about 5 s
+    t0 = time.perf_counter()
+    oracle.attend_rows(q_rows[:n_thr], k, v, rows[:n_thr], w.causal)
+    per_row = (time.perf_counter() - t0) / n_thr
+    n = int(max(n_thr, min(len(rows), 5.0 / max(per_row, 1e-6) * n_thr / n_thr)))
+    n = min(len(rows), max(n_thr, (n // n_thr) * n_thr))
+    times, fl = [], oracle.rows_flops(rows[:n], w.T, w.d, w.causal)
+    for s in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.attend_rows(q_rows[:n], k, v, rows[:n], w.causal)
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = fl * len(times) / tot / 1e12
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot / len(times) * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "N": w.N,
+                       "causal": w.causal, "input_dtype": w.dtype},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": n_thr, "kind": "oracle",
+                             "sample": f"{n} sampled query rows of one head per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="rsa", choices=["rsa", "reference"])
+    ap.add_argument("--workload", default="page1_causal_bf16")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--shape", default=None,
+                    help="B,H,T,d,N,causal: a bf16 normal-recipe workload instead of --workload (profiling)")
+    args = ap.parse_args()
+
+    import rsa_inputs
+    w = rsa_inputs.WORKLOADS[args.workload]
+    if args.shape:
+        B_, H_, T_, d_, N_, c_ = (int(x) for x in args.shape.split(","))
+        w = rsa_inputs.Workload(f"custom_B{B_}_H{H_}_T{T_}_d{d_}_N{N_}_{'causal' if c_ else 'full'}",
+                                B_, H_, T_, d_, N_, bool(c_), "bf16", "normal", "sample")
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import numpy as np
+    import torch
+    import context_attention_rsa_gb300 as rsa
+
+    world, rank, local = dist_info()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    rsa.load()
+
+    q, k, v = rsa_inputs.make_workload(w, seed=rank, device=dev)
+    B, H, T, d, N, causal = w.B, w.H, w.T, w.d, w.N, w.causal
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(rsa.workspace_size(q.dtype, B, H, T, d, N, causal), 1), dtype=torch.uint8, device=dev)
+    n_launch = rsa.ring_launch_count(N, causal)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    for _ in range(max(args.warmup, 0)):
+        rsa.ring_attn(q, k, v, N, causal, out=out, lse=lse, workspace=ws)
+    torch.cuda.synchronize()
+    rsa.check_device_error()
+
+    ev0 = [[torch.cuda.Event(enable_timing=True) for _ in range(n_launch)] for _ in range(args.steps)]
+    ev1 = [[torch.cuda.Event(enable_timing=True) for _ in range(n_launch)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    kinds = None
+    for s in range(args.steps):
+        kinds = rsa.ring_attn_timed(q, k, v, N, causal, out, lse, ws, ev0[s], ev1[s])
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    rsa.check_device_error()
+    ms_total = t_start.elapsed_time(t_stop)
+    if pg is not None:
+        tt = torch.tensor([ms_total], device=dev)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+
+    blk_ms = sum(ev0[s][i].elapsed_time(ev1[s][i]) for s in range(args.steps) for i in range(n_launch)
+                 if kinds[i] == 0) / args.steps
+    mrg_ms = sum(ev0[s][i].elapsed_time(ev1[s][i]) for s in range(args.steps) for i in range(n_launch)
+                 if kinds[i] == 1) / args.steps
+    n_blk = sum(1 for x in kinds if x == 0)
+    n_mrg = sum(1 for x in kinds if x == 1)
+
+    flops = useful_flops(B, H, T, d, causal)
+    value = flops * world / (ms_step * 1e-3) / 1e12
+    peaks = read_peaks()
+    blk_tflops = flops / (blk_ms * 1e-3) / 1e12
+    mbytes = merge_bytes_per_step(w, lambda r: rsa.ring_schedule(N, causal, r))
+    mrg_gbs = mbytes / (mrg_ms * 1e-3) / 1e9 if mrg_ms > 0 else None
+
+    # ---- end to end from pinned host memory (public API) --------------------
+    e2e = None
+    if args.e2e_steps > 0:
+        qh = q.cpu().pin_memory()
+        kh = k.cpu().pin_memory()
+        vh = v.cpu().pin_memory()
+        del q, k, v, out, lse, ws
+        torch.cuda.empty_cache()
+        bufs = None
+        _, _, bufs = rsa.ring_attn_from_host(qh, kh, vh, N, causal, device=dev)  # warm-up
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            rsa.ring_attn_from_host(qh, kh, vh, N, causal, device=dev, buffers=bufs)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        if pg is not None:
+            tt = torch.tensor([e_ms], device=dev)
+            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        h2d = 3 * qh.numel() * qh.element_size()
+        d2h = bufs["out_host"].numel() * bufs["out_host"].element_size() + bufs["lse_host"].numel() * 4
+        e2e = {"value": flops * world / (e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        k_cpu, v_cpu, q_cpu = kh, vh, qh
+    else:
+        q_cpu, k_cpu, v_cpu = q.cpu(), k.cpu(), v.cpu()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows = rsa_inputs.sample_rows(w, n=4096, seed=1)
+        qa = q_cpu.view(torch.int16).numpy().view(np.uint16) if q_cpu.dtype == torch.bfloat16 else q_cpu.numpy()
+        q_rows = np.ascontiguousarray(qa[rows[:, 0], rows[:, 1], rows[:, 2]])
+        rng = np.random.default_rng(2)
+        perm = rng.permutation(len(rows))
+        cpu = cpu_baseline(w, q_rows[perm], k_cpu, v_cpu, rows[perm], budget_s=args.cpu_budget_s)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "H": H, "T": T, "d": d, "N": N, "causal": causal,
+                       "global_batch": B * world, "seq_len": T, "parallelism": f"replicas{world}",
+                       "l2": "inputs (3 x %.1f GiB) larger than L2; no flush" % (q_cpu.numel() * 2 / 2**30)},
+            "pct_bf16_peak": 100.0 * value / world / peaks["bf16_tflops_sustained"],
+            "roofline": {"bound": "tensor", "achieved": blk_tflops, "peak": peaks["bf16_tflops_sustained"],
+                         "unit": "TFLOP/s", "frac": blk_tflops / peaks["bf16_tflops_sustained"],
+                         "traffic": None, "kernel": "block_attn_bf16_kernel<128>",
+                         "launches_per_step": n_blk, "ms_per_step": blk_ms,
+                         "peak_source": peaks["source"] + " bf16_tflops_sustained"},
+            "merge": {"bound": "hbm", "achieved": mrg_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                      "frac": (mrg_gbs / peaks["hbm_gbs"]) if mrg_gbs else None,
+                      "algorithmic_bytes_per_step": mbytes, "launches_per_step": n_mrg, "ms_per_step": mrg_ms,
+                      "peak_source": peaks["source"] + " hbm_gbs"},
+            "e2e": e2e,
+            "gpu_launches": n_launch * args.steps,
+            "cpu_baseline": cpu,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,286 @@
+"""Blockwise ring self-attention (forward) on one NVIDIA GB300.
+
+A thin ctypes binding over ``librsa.so`` (the C ABI in ``include/rsa.h``).  It
+only marshals arguments: torch tensors supply device memory and the current
+stream; every step of the attention path runs in the library's CUDA kernels.
+There is no CPU fallback -- if the library cannot be built or loaded, every
+call raises.
+
+Pages: "Sequence parallelism -- splitting the token dimension across GPUs"
+(llmdaily, day 58): chunking ("Split tokens across four GPUs"), the ring
+("A better mental model: move blocks past the queries"), online softmax ("But
+softmax seems to require all attention scores at once") and causal skipping
+("Causal attention gives us another optimization").
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+from typing import List, Optional, Sequence, Tuple
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "RsaError", "load", "library_path", "block_attn_fwd", "merge", "merge_finalize",
+    "ring_attn", "ring_attn_timed", "ring_attn_from_host", "workspace_size", "ring_schedule",
+    "set_wait_limit_ns", "check_device_error", "selftest_wait_timeout", "version",
+    "RSA_F32", "RSA_BF16",
+]
+
+RSA_F32 = 0
+RSA_BF16 = 1
+_STATUS = {0: "RSA_OK", 1: "RSA_ERR_INVALID_ARG", 2: "RSA_ERR_UNSUPPORTED", 3: "RSA_ERR_CUDA",
+           4: "RSA_ERR_TIMEOUT"}
+
+
+class RsaError(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str):
+        super().__init__(f"{fn}: {_STATUS.get(status, status)}: {detail}")
+        self.status = status
+        self.fn = fn
+
+
+_lib = None
+_lock = threading.Lock()
+
+_c_void_p = ctypes.c_void_p
+_i32 = ctypes.c_int
+_i64 = ctypes.c_int64
+
+_SIGS = {
+    "rsa_block_attn_fwd": [_c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _i64, _i32,
+                           _i64, _i64, _i64, _i64, _i32, _c_void_p, _c_void_p, _c_void_p],
+    "rsa_merge": [_c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _i64, _i32, _c_void_p],
+    "rsa_merge_finalize": [_c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p, _i64, _i32,
+                           _c_void_p, _i32, _c_void_p, _c_void_p],
+    "rsa_ring_attn_workspace_size": [_i32, _i32, _i32, _i64, _i32, _i32, _i32,
+                                     ctypes.POINTER(ctypes.c_size_t)],
+    "rsa_ring_attn_fwd": [_c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _i64, _i32, _i32, _i32,
+                          _c_void_p, _c_void_p, _c_void_p, ctypes.c_size_t, _c_void_p],
+    "rsa_ring_attn_fwd_timed": [_c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _i64, _i32, _i32,
+                                _i32, _c_void_p, _c_void_p, _c_void_p, ctypes.c_size_t, _c_void_p,
+                                ctypes.POINTER(_c_void_p), ctypes.POINTER(_c_void_p),
+                                ctypes.POINTER(_i32), _i32, ctypes.POINTER(_i32)],
+    "rsa_ring_schedule": [_i32, _i32, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _i32,
+                          ctypes.POINTER(_i32)],
+    "rsa_set_wait_limit_ns": [ctypes.c_uint64],
+    "rsa_check_device_error": [_c_void_p],
+    "rsa_selftest_wait_timeout": [_c_void_p],
+    "rsa_status_string": [_i32],
+    "rsa_last_error_string": [],
+    "rsa_version": [],
+}
+
+
+def library_path(build: bool = True) -> str:
+    return _build.build() if build else _build.LIB
+
+
+def load(build: bool = True):
+    """Load librsa.so (building it in-tree first if it is stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path(build)
+            lib = ctypes.CDLL(path)
+            for name, args in _SIGS.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_char_p if name in ("rsa_status_string", "rsa_last_error_string") \
+                    else ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _call(name: str, *args) -> None:
+    lib = load()
+    st = getattr(lib, name)(*args)
+    if st != 0:
+        detail = lib.rsa_last_error_string()
+        raise RsaError(name, st, detail.decode() if detail else "")
+
+
+def version() -> int:
+    return int(load().rsa_version())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return RSA_F32
+    if t.dtype == torch.bfloat16:
+        return RSA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _check_qkv(q, k, v) -> Tuple[int, int, int, int]:
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, H, T, d] tensor")
+    if not (q.shape == k.shape == v.shape) or not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share shape and dtype")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must live on one device")
+    B, H, T, d = q.shape
+    return B, H, T, d
+
+
+def workspace_size(dtype: torch.dtype, B: int, H: int, T: int, d: int, N: int, causal: bool) -> int:
+    n = ctypes.c_size_t(0)
+    dt = RSA_F32 if dtype == torch.float32 else RSA_BF16
+    _call("rsa_ring_attn_workspace_size", dt, B, H, T, d, N, int(bool(causal)), ctypes.byref(n))
+    return int(n.value)
+
+
+def block_attn_fwd(q, k, v, q_off: int, q_len: int, kv_off: int, kv_len: int, causal: bool,
+                   o_blk: Optional[torch.Tensor] = None, lse_blk: Optional[torch.Tensor] = None,
+                   stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """One (query chunk, KV chunk) pair: (o_blk [B, H, q_len, d], lse_blk [B, H, q_len])."""
+    B, H, T, d = _check_qkv(q, k, v)
+    if o_blk is None:
+        o_blk = torch.empty((B, H, q_len, d), dtype=q.dtype, device=q.device)
+    if lse_blk is None:
+        lse_blk = torch.empty((B, H, q_len), dtype=torch.float32, device=q.device)
+    _call("rsa_block_attn_fwd", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d,
+          q_off, q_len, kv_off, kv_len, int(bool(causal)), o_blk.data_ptr(), lse_blk.data_ptr(),
+          _stream(stream))
+    return o_blk, lse_blk
+
+
+def merge(o_acc: torch.Tensor, lse_acc: torch.Tensor, o_blk: torch.Tensor, lse_blk: torch.Tensor,
+          stream=None) -> None:
+    """In place: (o_acc, lse_acc) <- merge((o_acc, lse_acc), (o_blk, lse_blk))."""
+    d = o_acc.shape[-1]
+    rows = lse_acc.numel()
+    if o_acc.dtype != torch.float32 or lse_acc.dtype != torch.float32 or lse_blk.dtype != torch.float32:
+        raise TypeError("o_acc, lse_acc and lse_blk must be float32")
+    if o_blk.numel() != rows * d or o_acc.numel() != rows * d or lse_blk.numel() != rows:
+        raise ValueError("row counts differ")
+    for t in (o_acc, lse_acc, o_blk, lse_blk):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("merge operands must be contiguous CUDA tensors")
+    _call("rsa_merge", o_acc.data_ptr(), lse_acc.data_ptr(), o_blk.data_ptr(), _dt(o_blk),
+          lse_blk.data_ptr(), rows, d, _stream(stream))
+
+
+def merge_finalize(o_acc, lse_acc, o_blk, lse_blk, out_dtype=torch.bfloat16, out=None, lse_out=None,
+                   stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    d = o_acc.shape[-1]
+    rows = lse_acc.numel()
+    if o_blk.numel() != rows * d or o_acc.numel() != rows * d or lse_blk.numel() != rows:
+        raise ValueError("row counts differ")
+    if out is None:
+        out = torch.empty(o_acc.shape, dtype=out_dtype, device=o_acc.device)
+    if lse_out is None:
+        lse_out = torch.empty(lse_acc.shape, dtype=torch.float32, device=o_acc.device)
+    _call("rsa_merge_finalize", o_acc.data_ptr(), lse_acc.data_ptr(), o_blk.data_ptr(), _dt(o_blk),
+          lse_blk.data_ptr(), rows, d, out.data_ptr(), _dt(out), lse_out.data_ptr(), _stream(stream))
+    return out, lse_out
+
+
+def ring_attn(q, k, v, N: int, causal: bool, out=None, lse=None, workspace=None,
+              stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The whole ring: (out [B, H, T, d] in q's dtype, lse [B, H, T] fp32)."""
+    B, H, T, d = _check_qkv(q, k, v)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    need = workspace_size(q.dtype, B, H, T, d, N, causal)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _call("rsa_ring_attn_fwd", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
+          int(bool(causal)), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+          workspace.numel() * workspace.element_size(), _stream(stream))
+    return out, lse
+
+
+def ring_attn_timed(q, k, v, N: int, causal: bool, out, lse, workspace, events_start: Sequence,
+                    events_stop: Sequence, stream=None) -> List[int]:
+    """ring_attn that records the given torch.cuda.Event pairs around each
+    kernel launch; returns the launch kinds (0 block attention, 1 merge)."""
+    B, H, T, d = _check_qkv(q, k, v)
+    cap = len(events_start)
+    st = torch.cuda.current_stream() if stream is None else stream
+    for e in list(events_start) + list(events_stop):
+        if not e.cuda_event:  # torch creates the CUDA event on first record
+            e.record(st)
+    ev_s = (ctypes.c_void_p * cap)(*[int(e.cuda_event) for e in events_start])
+    ev_e = (ctypes.c_void_p * cap)(*[int(e.cuda_event) for e in events_stop])
+    kinds = (ctypes.c_int * cap)()
+    n = ctypes.c_int(0)
+    _call("rsa_ring_attn_fwd_timed", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
+          int(bool(causal)), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+          workspace.numel() * workspace.element_size(), _stream(stream), ev_s, ev_e, kinds, cap,
+          ctypes.byref(n))
+    return [kinds[i] for i in range(n.value)]
+
+
+def ring_launch_count(N: int, causal: bool) -> int:
+    """Kernel launches one ring makes (block-attention plus merge launches)."""
+    n = 0
+    for r in range(N):
+        np_ = len(ring_schedule(N, causal, r))
+        groups = (np_ + 31) // 32
+        n += groups if r == 0 else 2 * groups
+    return n
+
+
+def ring_attn_from_host(q_host, k_host, v_host, N: int, causal: bool, device=None, stream=None,
+                        buffers=None):
+    """End-to-end call from host memory: copy Q, K, V (ideally pinned) to the
+    device, run the ring, and copy out and lse back into host tensors.
+    ``buffers`` may hold reusable device/host tensors (q, k, v, out, lse, ws,
+    out_host, lse_host) to keep allocation out of a timed loop."""
+    dev = torch.device(device) if device is not None else torch.device("cuda")
+    b = buffers if buffers is not None else {}
+    B, H, T, d = q_host.shape
+    if "q" not in b:
+        b["q"] = torch.empty(q_host.shape, dtype=q_host.dtype, device=dev)
+        b["k"] = torch.empty(q_host.shape, dtype=q_host.dtype, device=dev)
+        b["v"] = torch.empty(q_host.shape, dtype=q_host.dtype, device=dev)
+        b["out"] = torch.empty(q_host.shape, dtype=q_host.dtype, device=dev)
+        b["lse"] = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+        b["ws"] = torch.empty(max(workspace_size(q_host.dtype, B, H, T, d, N, causal), 1),
+                              dtype=torch.uint8, device=dev)
+        b["out_host"] = torch.empty(q_host.shape, dtype=q_host.dtype, pin_memory=True)
+        b["lse_host"] = torch.empty((B, H, T), dtype=torch.float32, pin_memory=True)
+    b["q"].copy_(q_host, non_blocking=True)
+    b["k"].copy_(k_host, non_blocking=True)
+    b["v"].copy_(v_host, non_blocking=True)
+    ring_attn(b["q"], b["k"], b["v"], N, causal, out=b["out"], lse=b["lse"], workspace=b["ws"],
+              stream=stream)
+    b["out_host"].copy_(b["out"], non_blocking=True)
+    b["lse_host"].copy_(b["lse"], non_blocking=True)
+    return b["out_host"], b["lse_host"], b
+
+
+def ring_schedule(N: int, causal: bool, rnd: int) -> List[Tuple[int, int]]:
+    """Pairs (q_chunk, kv_chunk) of round rnd as the library schedules them."""
+    cap = max(N, 1)
+    qi = (ctypes.c_int * cap)()
+    kj = (ctypes.c_int * cap)()
+    n = ctypes.c_int(0)
+    _call("rsa_ring_schedule", N, int(bool(causal)), rnd, qi, kj, cap, ctypes.byref(n))
+    return [(qi[i], kj[i]) for i in range(n.value)]
+
+
+def set_wait_limit_ns(limit_ns: int) -> None:
+    _call("rsa_set_wait_limit_ns", int(limit_ns))
+
+
+def check_device_error(stream=None) -> None:
+    _call("rsa_check_device_error", _stream(stream))
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    _call("rsa_selftest_wait_timeout", _stream(stream))

@@ -1,0 +1,473 @@
+// Block attention on the sm_103a tensor cores: one launch computes, for every
+// (query chunk, KV chunk) pair it is given, o_blk = softmax(Q_i K_j^T / sqrt(d)) V_j
+// and the row log-sum-exp.
+//
+// Pages: "Sequence parallelism -- splitting the token dimension across GPUs"
+// (llmdaily, day 58): the attention equation of "Attention wants keys and
+// values from other tokens", the running (m, l, o) statistics and the
+// e^{m - m_new} rescale of "But softmax seems to require all attention scores
+// at once" (applied here between 128-key tiles inside one pair), and the
+// lower-triangular mask of "Causal attention gives us another optimization".
+//
+// Design (one CTA = 256 query rows of one pair and one head, as two 128-row
+// tiles that share every K/V tile):
+//   warp 8      TMA producer: Q tiles once, then K(j), V(j) through a ring of
+//               shared-memory slots (128-byte swizzle).
+//   warp 9      TMEM allocator and the single MMA-issuing thread:
+//                 S_t = Q_t K_j^T   (tcgen05.mma, A and B from shared memory)
+//                 O_t += P_t V_j    (tcgen05.mma, A = P from TMEM, B = V from
+//                                    shared memory, MN-major)
+//   warps 0-7   softmax, one thread per query row (TMEM lane = row): reads a
+//               row of S from TMEM, masks, takes the row max, rescales O when
+//               the max rose by more than 2^8, writes P = 2^{x - m} as bf16
+//               back over S, and finally writes o = O / l and
+//               lse = (m + log2 l) ln 2.
+// TMEM: S0 | S1 | O0 | O1 (128 + 128 + d + d columns of the 512).
+// The kept maximum m only moves when the new one exceeds it by more than 8
+// (log2 units); o, l and lse all use the same m, so the result is exact up to
+// rounding whatever m is kept.
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "ptx_sm103.cuh"
+#include "rsa_internal.h"
+
+namespace rsa {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 256x
+
+template <int D>
+struct Cfg {
+    static constexpr int kBoxes = D / 64;            // 128-byte-wide TMA boxes per tile
+    static constexpr uint32_t kBoxBytes = 128u * 128u; // 128 rows x 128 bytes
+    static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
+    static constexpr int kStages = D == 128 ? 4 : 6;
+    static constexpr uint32_t kQOff = 0;
+    static constexpr uint32_t kKVOff = 2 * kTileBytes;
+    static constexpr uint32_t kBarOff = kKVOff + kStages * kTileBytes;
+    static constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;
+    static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+    // barrier indices
+    static constexpr int kQF = 0;
+    static constexpr int kKVF = 1;
+    static constexpr int kKVE = kKVF + kStages;
+    static constexpr int kSF = kKVE + kStages;
+    static constexpr int kPF = kSF + 2;
+    static constexpr int kOF = kPF + 2;
+    static constexpr int kDrain = kOF + 2;
+    static constexpr int kNumBars = kDrain + 1;
+    static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
+};
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Keep uses of r[0..31] after a preceding volatile asm (the TMEM load wait).
+__device__ __forceinline__ void tie32(uint32_t *r)
+{
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        asm volatile("" : "+r"(r[i]));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    block_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v,
+                           const __grid_constant__ BlockParams p)
+{
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t sQ = base + C::kQOff;
+    const uint32_t sKV = base + C::kKVOff;
+    const uint32_t bars = base + C::kBarOff;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + C::kBarOff + 8 * C::kNumBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + C::kBarOff + 8 * C::kNumBars + 4);
+    auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---- which pair, head and 256-row group ------------------------------------
+    const int64_t BH = (int64_t)p.B * p.H;
+    const int64_t per_group = (int64_t)p.npairs * BH;
+    const int64_t L = blockIdx.x;
+    const int qg = p.n_qgroups - 1 - (int)(L / per_group);  // heaviest causal groups first
+    const int64_t rest = L % per_group;
+    const int pi = (int)(rest / BH);
+    const int bh = (int)(rest % BH);
+    const PairDesc &pr = p.pairs[pi];
+    const int64_t q0 = (int64_t)qg * kBf16RowsPerCta;
+    const int64_t rows_valid = min((int64_t)kBf16RowsPerCta, p.q_len - q0);
+    int64_t kv_end = p.kv_len;
+    if (p.causal)
+        kv_end = min(kv_end, pr.q_off + q0 + rows_valid - pr.kv_off);
+    const int n = kv_end > 0 ? (int)((kv_end + 127) / 128) : 0;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(BAR(C::kQF), 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            ptx::mbar_init(BAR(C::kKVF + s), 1);
+            ptx::mbar_init(BAR(C::kKVE + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(BAR(C::kSF + t), 1);
+            ptx::mbar_init(BAR(C::kPF + t), 128);
+            ptx::mbar_init(BAR(C::kOF + t), 1);
+        }
+        ptx::mbar_init(BAR(C::kDrain), 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 9) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    if (warp == 8 && lane == 0) {
+        ptx::tma_prefetch_desc(&tm_q);
+        ptx::tma_prefetch_desc(&tm_k);
+        ptx::tma_prefetch_desc(&tm_v);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint64_t lim_ns = p.wait_limit_ns;
+
+    if (warp == 8) {
+        // =========================== TMA producer ===========================
+        if (lane == 0 && n > 0) {
+            int last_use[C::kStages];
+            for (int s = 0; s < C::kStages; ++s)
+                last_use[s] = -1;
+            ptx::mbar_arrive_expect_tx(BAR(C::kQF), 2 * C::kTileBytes);
+            for (int t = 0; t < 2; ++t)
+                for (int b = 0; b < C::kBoxes; ++b)
+                    ptx::tma_load_3d(sQ + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, BAR(C::kQF),
+                                     b * 64, (int)(pr.q_off + q0 + t * 128), bh);
+            for (int ld = 0; ld < 2 * n; ++ld) {
+                const int slot = ld % C::kStages;
+                const int use = ld / C::kStages;
+                if (use > 0 &&
+                    !ptx::mbar_wait(BAR(C::kKVE + slot), (use - 1) & 1, lim_ns, abort_flag, p.err, 1))
+                    break;
+                const CUtensorMap *m = (ld & 1) ? &tm_v : &tm_k;
+                const int row = (int)(pr.kv_off + (int64_t)(ld >> 1) * 128);
+                ptx::mbar_arrive_expect_tx(BAR(C::kKVF + slot), C::kTileBytes);
+                for (int b = 0; b < C::kBoxes; ++b)
+                    ptx::tma_load_3d(sKV + slot * C::kTileBytes + b * C::kBoxBytes, m,
+                                     BAR(C::kKVF + slot), b * 64, row, bh);
+                last_use[slot] = use;
+            }
+            // Let every copy this thread started land before the CTA can exit.
+            volatile int no_abort = 0;
+            ptx::mbar_wait(BAR(C::kQF), 0, lim_ns, &no_abort, p.err, 2);
+            for (int s = 0; s < C::kStages; ++s)
+                if (last_use[s] >= 0)
+                    ptx::mbar_wait(BAR(C::kKVF + s), last_use[s] & 1, lim_ns, &no_abort, p.err, 3);
+        }
+    } else if (warp == 9) {
+        // ============================ MMA issuer ============================
+        if (lane == 0 && n > 0) {
+            const uint32_t idesc_qk = ptx::idesc_bf16_f32(128, 128, false);
+            const uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, true);
+            auto issue_qk = [&](int t, int slot) {
+                const uint32_t qa = sQ + t * C::kTileBytes;
+                const uint32_t kb = sKV + slot * C::kTileBytes;
+                const uint32_t dst = tmem + (t ? C::kColS1 : C::kColS0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+                    ptx::mma_ss(dst, ptx::smem_desc_sw128(qa + off, 16, 1024),
+                                ptx::smem_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
+                }
+            };
+            auto issue_pv = [&](int t, int slot, bool acc) {
+                const uint32_t vb = sKV + slot * C::kTileBytes;
+                const uint32_t dst = tmem + (t ? C::kColO1 : C::kColO0);
+                const uint32_t pa = tmem + (t ? C::kColS1 : C::kColS0);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    ptx::mma_ts(dst, pa + kk * 8, ptx::smem_desc_sw128(vb + kk * 2048, C::kBoxBytes, 1024),
+                                idesc_pv, (acc || kk > 0) ? 1u : 0u);
+            };
+            bool ok = ptx::mbar_wait(BAR(C::kQF), 0, lim_ns, abort_flag, p.err, 10);
+            int kslot = 0;
+            if (ok)
+                ok = ptx::mbar_wait(BAR(C::kKVF + 0), 0, lim_ns, abort_flag, p.err, 11);
+            if (ok) {
+                issue_qk(0, 0);
+                ptx::mma_commit(BAR(C::kSF + 0));
+                issue_qk(1, 0);
+                ptx::mma_commit(BAR(C::kSF + 1));
+                ptx::mma_commit(BAR(C::kKVE + 0));
+            }
+            for (int j = 0; ok && j < n; ++j) {
+                const int vld = 2 * j + 1;
+                const int vslot = vld % C::kStages;
+                ok = ptx::mbar_wait(BAR(C::kKVF + vslot), (vld / C::kStages) & 1, lim_ns, abort_flag, p.err, 12);
+                if (!ok)
+                    break;
+                // tile 0
+                ok = ptx::mbar_wait(BAR(C::kPF + 0), j & 1, lim_ns, abort_flag, p.err, 13);
+                if (!ok)
+                    break;
+                ptx::tc_fence_after();
+                issue_pv(0, vslot, j > 0);
+                const bool more = j + 1 < n;
+                if (more) {
+                    const int kld = 2 * (j + 1);
+                    kslot = kld % C::kStages;
+                    ok = ptx::mbar_wait(BAR(C::kKVF + kslot), (kld / C::kStages) & 1, lim_ns, abort_flag,
+                                        p.err, 14);
+                    if (!ok)
+                        break;
+                    issue_qk(0, kslot);
+                    ptx::mma_commit(BAR(C::kSF + 0));
+                } else {
+                    ptx::mma_commit(BAR(C::kOF + 0));
+                }
+                // tile 1
+                ok = ptx::mbar_wait(BAR(C::kPF + 1), j & 1, lim_ns, abort_flag, p.err, 15);
+                if (!ok)
+                    break;
+                ptx::tc_fence_after();
+                issue_pv(1, vslot, j > 0);
+                ptx::mma_commit(BAR(C::kKVE + vslot));
+                if (more) {
+                    issue_qk(1, kslot);
+                    ptx::mma_commit(BAR(C::kSF + 1));
+                    ptx::mma_commit(BAR(C::kKVE + kslot));
+                } else {
+                    ptx::mma_commit(BAR(C::kOF + 1));
+                }
+            }
+            // Drain: every MMA this thread issued has finished before TMEM is freed.
+            ptx::mma_commit(BAR(C::kDrain));
+            volatile int no_abort = 0;
+            ptx::mbar_wait(BAR(C::kDrain), 0, lim_ns, &no_abort, p.err, 16);
+        }
+        __syncwarp();
+    } else {
+        // ============================== softmax ==============================
+        const int t = warp >> 2;
+        const int wi = warp & 3;
+        const int row = wi * 32 + lane;
+        const int64_t rg = q0 + t * 128 + row;  // row inside the pair
+        const int64_t qpos = pr.q_off + rg;
+        const uint32_t lane_addr = (uint32_t)(wi * 32) << 16;
+        const uint32_t tS = tmem + lane_addr + (t ? C::kColS1 : C::kColS0);
+        const uint32_t tO = tmem + lane_addr + (t ? C::kColO1 : C::kColO0);
+        const float sl2 = 1.4426950408889634f / sqrtf((float)D);  // log2(e) / sqrt(d)
+        int64_t allowed = p.kv_len;  // keys [0, allowed) of the pair are visible to this row
+        if (p.causal)
+            allowed = min(allowed, qpos - pr.kv_off + 1);
+        float m_used = -INFINITY;  // kept maximum, log2 units
+        float l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n; ++j) {
+            ok = ptx::mbar_wait(BAR(C::kSF + t), j & 1, lim_ns, abort_flag, p.err, 20);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok)
+                break;
+            ptx::tc_fence_after();
+            uint32_t s[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                ptx::tmem_ld32(tS + c * 32, s + c * 32);
+            ptx::tmem_ld_wait(s);
+            tie32(s + 32);
+            tie32(s + 64);
+            tie32(s + 96);
+            const int64_t lim = allowed - (int64_t)j * 128;
+            float mx = -INFINITY;
+            if (lim >= 128) {
+#pragma unroll
+                for (int i = 0; i < 128; ++i)
+                    mx = fmaxf(mx, u2f(s[i]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 128; ++i) {
+                    if ((int64_t)i >= lim)
+                        s[i] = f2u(-INFINITY);
+                    mx = fmaxf(mx, u2f(s[i]));
+                }
+            }
+            const float mnew = mx * sl2;
+            const bool need = (mnew > -INFINITY) && (m_used == -INFINITY || mnew > m_used + kRescaleThreshold);
+            if (__any_sync(0xffffffffu, need)) {
+                float alpha = 1.f;
+                if (need) {
+                    alpha = (m_used == -INFINITY) ? 0.f : ptx::ex2(m_used - mnew);
+                    l *= alpha;
+                    m_used = mnew;
+                }
+                if (j > 0) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32(tO + c * 32, o);
+                        ptx::tmem_ld_wait(o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            o[i] = f2u(u2f(o[i]) * alpha);
+                        ptx::tmem_st32(tO + c * 32, o);
+                    }
+                    ptx::tmem_st_wait();
+                }
+            }
+            const float neg = (m_used == -INFINITY) ? 0.f : -m_used;
+            float sum = 0.f;
+            uint32_t pk[64];
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const float p0 = ptx::ex2(fmaf(u2f(s[2 * i]), sl2, neg));
+                const float p1 = ptx::ex2(fmaf(u2f(s[2 * i + 1]), sl2, neg));
+                sum += p0 + p1;
+                pk[i] = pack_bf16(p0, p1);
+            }
+            l += sum;
+            ptx::tmem_st32(tS, pk);
+            ptx::tmem_st32(tS + 32, pk + 32);
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(BAR(C::kPF + t));
+        }
+        if (ok && n > 0) {
+            ok = ptx::mbar_wait(BAR(C::kOF + t), 0, lim_ns, abort_flag, p.err, 21);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+            ptx::tc_fence_after();
+            const bool empty = !(l > 0.f);
+            const float inv = empty ? 0.f : 1.f / l;
+            const bool valid = rg < p.q_len;
+            const int64_t orow = (int64_t)bh * pr.out_T + pr.out_t0 + rg;
+            if (valid)
+                pr.lse[orow] = empty ? -INFINITY : (m_used + ptx::lg2(l)) * 0.69314718055994531f;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                if (n > 0) {
+                    ptx::tmem_ld32(tO + c * 32, o);
+                    ptx::tmem_ld_wait(o);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        o[i] = 0u;
+                }
+                if (valid) {
+                    if (pr.out_f32) {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(pr.out) + orow * D + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(u2f(o[4 * i]) * inv, u2f(o[4 * i + 1]) * inv,
+                                                 u2f(o[4 * i + 2]) * inv, u2f(o[4 * i + 3]) * inv);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.out) + orow * D + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(pack_bf16(u2f(o[8 * i]) * inv, u2f(o[8 * i + 1]) * inv),
+                                                pack_bf16(u2f(o[8 * i + 2]) * inv, u2f(o[8 * i + 3]) * inv),
+                                                pack_bf16(u2f(o[8 * i + 4]) * inv, u2f(o[8 * i + 5]) * inv),
+                                                pack_bf16(u2f(o[8 * i + 6]) * inv, u2f(o[8 * i + 7]) * inv));
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- teardown --------------------------------------------------------------
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// [B*H, T, d] bf16 view with 128-row x 64-column boxes and 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t BH, int64_t T, int d)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_d(const void *q, const void *k, const void *v, const BlockParams &p, cudaStream_t s)
+{
+    const int64_t BH = (int64_t)p.B * p.H;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, q, BH, p.T, D) || !make_map(&mk, k, BH, p.T, D) || !make_map(&mv, v, BH, p.T, D))
+        return cudaErrorInvalidValue;
+    const int64_t grid = (int64_t)p.n_qgroups * p.npairs * BH;
+    if (grid <= 0)
+        return cudaSuccess;
+    if (grid > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    const uint32_t smem = Cfg<D>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(block_attn_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    block_attn_bf16_kernel<D><<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_block_attn_bf16(const void *q, const void *k, const void *v, const BlockParams &p,
+                                   cudaStream_t s)
+{
+    if (p.d == 128)
+        return launch_d<128>(q, k, v, p, s);
+    if (p.d == 64)
+        return launch_d<64>(q, k, v, p, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace rsa

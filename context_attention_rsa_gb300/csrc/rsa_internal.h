@@ -1,0 +1,84 @@
+// Internal declarations shared by the librsa translation units: launch
+// parameter blocks, the launchers each kernel file exports, and status helpers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/rsa.h"
+
+namespace rsa {
+
+// Device error word values (OR-ed with a site code in the low byte).
+constexpr unsigned int kDevErrTimeout = 0x100u;
+
+// Most pairs one kernel launch takes; longer pair lists are split.
+constexpr int kMaxPairsPerLaunch = 32;
+
+// One (query chunk, KV chunk) pair inside a block-attention launch.  Output
+// row r of head bh goes to out[(bh * out_T + out_t0 + r) * d] and
+// lse[bh * out_T + out_t0 + r].
+struct PairDesc {
+    int64_t q_off;   // global position of the first query row
+    int64_t kv_off;  // global position of the first key
+    void *out;       // bf16 or fp32 (out_f32)
+    float *lse;
+    int64_t out_T;   // row pitch of out/lse per head
+    int64_t out_t0;  // first row of this pair inside each head
+    int out_f32;     // 1: fp32 output, 0: bf16 output
+    int pad_;
+};
+
+struct BlockParams {
+    int B, H;
+    int64_t T;
+    int d;
+    int causal;
+    int64_t q_len, kv_len;  // rows per pair, keys per pair
+    int npairs;
+    int n_qgroups;          // query-row groups per pair (rows per CTA granularity)
+    uint64_t wait_limit_ns;
+    unsigned int *err;      // device error word
+    PairDesc pairs[kMaxPairsPerLaunch];
+};
+
+// One pair's rows inside a merge launch.  Row rr (0 <= rr < rows_per_pair)
+// of the pair is head bh = rr / Tc, position t = rr % Tc; its accumulator row
+// is bh * T + acc_t0 + t and its partial row is rr.
+struct MergePair {
+    int64_t acc_t0;
+    const void *o_blk;
+    const float *lse_blk;
+    int final_;  // 1: write out/lse_out, 0: update o_acc/lse_acc in place
+    int pad_;
+};
+
+struct MergeParams {
+    int64_t rows_per_pair, Tc, T;
+    int npairs, d;
+    int blk_f32, out_f32;
+    float *o_acc;
+    float *lse_acc;
+    void *out;
+    float *lse_out;
+    MergePair pairs[kMaxPairsPerLaunch];
+};
+
+// Launchers (no validation; the C ABI layer validates).  They return the
+// cudaError_t of the launch.
+cudaError_t launch_block_attn_bf16(const void *q, const void *k, const void *v,
+                                   const BlockParams &p, cudaStream_t s);
+cudaError_t launch_block_attn_f32(const float *q, const float *k, const float *v,
+                                  const BlockParams &p, cudaStream_t s);
+cudaError_t launch_merge(const MergeParams &p, cudaStream_t s);
+cudaError_t launch_selftest_wait(uint64_t limit_ns, unsigned int *err, cudaStream_t s);
+
+// Rows of one CTA of the tensor-core kernel (two 128-row tiles).
+constexpr int kBf16RowsPerCta = 256;
+
+// Set the thread's last-error text and return `st`.
+rsa_status fail(rsa_status st, const char *fmt, ...);
+
+}  // namespace rsa

@@ -1,0 +1,178 @@
+/*
+ * rsa.h -- C ABI of librsa: blockwise ring self-attention (forward) on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Pages cited:
+ *   [P1] "Sequence parallelism -- splitting the token dimension across GPUs"
+ *        (llmdaily, day 58)
+ *   [P3] "Sequence Parallelism" (glossary entry, zhongzhoutan-coder terms)
+ *
+ * The sequence of length T is cut into N contiguous chunks of T/N tokens
+ * ([P1] "Split tokens across four GPUs").  Query chunks stay put while the
+ * key/value chunks are visited in ring order ([P1] "A better mental model:
+ * move blocks past the queries"); each (query chunk, KV chunk) pair gives a
+ * partial output and a row log-sum-exp, folded into the running result with
+ * the online-softmax rescale e^{m - m_new} ([P1] "But softmax seems to
+ * require all attention scores at once").  All N chunks live on one GPU; a
+ * ring step is a change of base address, not a copy.
+ *
+ * Conventions for every call:
+ *   - Tensors are dense row-major.  q, k, v and out are [B, H, T, d]
+ *     (d = d_k, the head dimension); lse is [B, H, T].  "Row" means one
+ *     (b, h, t) query row.
+ *   - Pointers named q, k, v, out, lse, o_*, lse_* and workspace are DEVICE
+ *     pointers on the current CUDA device, 16-byte aligned.  The caller owns
+ *     every buffer; the library allocates no device memory and keeps no state
+ *     beyond a device-side error word.
+ *   - Scores are scaled by 1/sqrt(d) ([P1] "Attention wants keys and values
+ *     from other tokens", the attention equation); the scale is not a
+ *     parameter.  lse is the natural-log log-sum-exp of the scaled scores.
+ *   - Causal means query position t sees keys 0..t inclusive ([P1] "Causal
+ *     attention gives us another optimization"; the page's token 30,000
+ *     attends to 1..30,000).
+ *   - Work is enqueued on `stream` (NULL = the legacy default stream) and is
+ *     asynchronous: results are valid once the stream has passed the call.
+ *     No call synchronises, except rsa_check_device_error.
+ *   - Arguments are validated before anything is launched, so a call that
+ *     returns RSA_ERR_INVALID_ARG or RSA_ERR_UNSUPPORTED has no side effect.
+ *     A failed launch returns RSA_ERR_CUDA.  A device-side wait that ran past
+ *     its time limit sets the device error word; rsa_check_device_error then
+ *     returns RSA_ERR_TIMEOUT.  Nothing aborts, exits or traps.
+ *   - rsa_last_error_string() describes the last failure on this thread.
+ *
+ * Supported shapes: fp32 inputs with d in {64, 128} (SIMT kernel), bf16
+ * inputs with d in {64, 128} (tcgen05 tensor-core kernel).
+ */
+#ifndef RSA_H
+#define RSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *rsa_stream_t; /* the same handle as cudaStream_t */
+typedef struct CUevent_st *rsa_event_t;   /* the same handle as cudaEvent_t */
+
+typedef enum {
+    RSA_OK = 0,
+    RSA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, N does not divide T ... */
+    RSA_ERR_UNSUPPORTED = 2, /* valid request this build does not serve (dtype, d, device) */
+    RSA_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed */
+    RSA_ERR_TIMEOUT = 4      /* a device wait exceeded its limit (see rsa_set_wait_limit_ns) */
+} rsa_status;
+
+typedef enum { RSA_F32 = 0, RSA_BF16 = 1 } rsa_dtype;
+
+/*
+ * One (query chunk, KV chunk) pair -- the block step of [P1] "A better mental
+ * model: move blocks past the queries": the queries q[:, :, q_off : q_off+q_len]
+ * attend to the keys/values k, v[:, :, kv_off : kv_off+kv_len]:
+ *   o_blk   = softmax(Q_i K_j^T / sqrt(d)) V_j       [B, H, q_len, d], dtype dt
+ *   lse_blk = log sum_j e^{s_j}                      [B, H, q_len], fp32
+ * q, k, v are the FULL [B, H, T, d] tensors; the offsets are global token
+ * positions, so the causal mask compares kv_off + c with q_off + r.  Rows with
+ * no allowed key get o_blk = 0 and lse_blk = -inf.
+ * Requires 0 <= q_off, q_off + q_len <= T, 0 <= kv_off, kv_off + kv_len <= T,
+ * q_len, kv_len >= 1.
+ */
+rsa_status rsa_block_attn_fwd(const void *q, const void *k, const void *v, rsa_dtype dt,
+                              int B, int H, int64_t T, int d,
+                              int64_t q_off, int64_t q_len, int64_t kv_off, int64_t kv_len,
+                              int causal, void *o_blk, float *lse_blk, rsa_stream_t stream);
+
+/*
+ * Online-softmax merge, in place, of [P1] "But softmax seems to require all
+ * attention scores at once" written for normalised partials:
+ *   a = lse_acc, b = lse_blk, M = max(a, b), L = M + ln(e^{a-M} + e^{b-M})
+ *   o_acc <- o_acc e^{a-L} + o_blk e^{b-L},   lse_acc <- L
+ * over `rows` contiguous rows of d values.  o_acc is fp32; o_blk has dtype
+ * blk_dt.  Two empty rows (both lse = -inf) stay empty: o = 0, lse = -inf.
+ */
+rsa_status rsa_merge(float *o_acc, float *lse_acc, const void *o_blk, rsa_dtype blk_dt,
+                     const float *lse_blk, int64_t rows, int d, rsa_stream_t stream);
+
+/*
+ * The same merge as rsa_merge, but the result is written to `out` (dtype
+ * out_dt, rounded to nearest even for bf16) and `lse_out` instead of back
+ * into the accumulator: the last merge of a ring.  o_acc/lse_acc are read
+ * only.  lse_out may alias lse_acc.
+ */
+rsa_status rsa_merge_finalize(const float *o_acc, const float *lse_acc, const void *o_blk,
+                              rsa_dtype blk_dt, const float *lse_blk, int64_t rows, int d,
+                              void *out, rsa_dtype out_dt, float *lse_out, rsa_stream_t stream);
+
+/*
+ * Bytes of device workspace rsa_ring_attn_fwd needs for this shape (written
+ * to *bytes): an fp32 accumulator for the chunks visited more than once plus
+ * room for one round's partial results.
+ */
+rsa_status rsa_ring_attn_workspace_size(rsa_dtype dt, int B, int H, int64_t T, int d, int N,
+                                        int causal, size_t *bytes);
+
+/*
+ * Whole ring on one GPU ([P1] "A better mental model: move blocks past the
+ * queries", with [P1] "Causal attention gives us another optimization"):
+ * round r pairs query chunk i with KV chunk (i - r) mod N; when causal, pairs
+ * whose KV chunk lies after the query chunk are skipped, leaving N(N+1)/2
+ * pairs.  Round 0 (the diagonal) writes straight into the accumulator (or into
+ * out/lse for a chunk visited once); every later round computes its pairs'
+ * partials and merges them; a chunk's last merge writes out (dtype dt) and
+ * lse.  Requires N >= 1 and N dividing T.  `workspace` must hold
+ * rsa_ring_attn_workspace_size() bytes.
+ */
+rsa_status rsa_ring_attn_fwd(const void *q, const void *k, const void *v, rsa_dtype dt,
+                             int B, int H, int64_t T, int d, int N, int causal,
+                             void *out, float *lse, void *workspace, size_t ws_bytes,
+                             rsa_stream_t stream);
+
+/*
+ * rsa_ring_attn_fwd with profiling: before and after each kernel launch it
+ * records ev_start[i] / ev_stop[i] on `stream` and sets kind[i] to 0 for a
+ * block-attention launch or 1 for a merge launch.  `cap` is the length of the
+ * three arrays (host memory; the events are created by the caller); the number
+ * of launches is written to *n_launches (the call fails with
+ * RSA_ERR_INVALID_ARG, before launching anything, if cap is too small).
+ */
+rsa_status rsa_ring_attn_fwd_timed(const void *q, const void *k, const void *v, rsa_dtype dt,
+                                   int B, int H, int64_t T, int d, int N, int causal,
+                                   void *out, float *lse, void *workspace, size_t ws_bytes,
+                                   rsa_stream_t stream, rsa_event_t *ev_start,
+                                   rsa_event_t *ev_stop, int *kind, int cap, int *n_launches);
+
+/*
+ * Host-only view of the ring schedule used by rsa_ring_attn_fwd: the pairs of
+ * round r (0-based) as (q_chunk[p], kv_chunk[p]) in host arrays of length
+ * `cap`; their count goes to *n_pairs.  No GPU needed.
+ */
+rsa_status rsa_ring_schedule(int N, int causal, int round, int *q_chunk, int *kv_chunk, int cap,
+                             int *n_pairs);
+
+/* Set the limit (nanoseconds, >= 1 ms) of every device-side wait; default 2 s. */
+rsa_status rsa_set_wait_limit_ns(uint64_t limit_ns);
+
+/*
+ * Synchronise `stream`, then read and clear the device error word of the
+ * current device: RSA_OK, or RSA_ERR_TIMEOUT if a kernel gave up on a wait.
+ */
+rsa_status rsa_check_device_error(rsa_stream_t stream);
+
+/*
+ * Self-test of the wait limit: launches one block that waits, with the
+ * current limit, on a shared-memory barrier nothing ever arrives at; the wait
+ * gives up and sets the device error word, which rsa_check_device_error
+ * reports as RSA_ERR_TIMEOUT.  The block then exits normally.
+ */
+rsa_status rsa_selftest_wait_timeout(rsa_stream_t stream);
+
+const char *rsa_status_string(rsa_status status);
+const char *rsa_last_error_string(void);
+int rsa_version(void); /* major * 10000 + minor * 100 + patch */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RSA_H */

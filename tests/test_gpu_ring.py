@@ -1,0 +1,173 @@
+"""GPU parity of the whole ring (rsa_ring_attn_fwd) against the oracle, with
+ragged and degenerate shapes, bit-exact invariants from the pages, and the
+device-side wait-limit self-test."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rsa_inputs
+import context_attention_rsa_gb300 as rsa
+from gpu_helpers import assert_close, need_cuda, qkv_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_fp32_causal_workload_all_rows():
+    need_cuda()
+    w = rsa_inputs.WORKLOADS["tiny_fp32_causal"]
+    q, k, v = rsa_inputs.make_workload(w, seed=0, device="cpu")
+    out, lse = rsa.ring_attn(q.cuda(), k.cuda(), v.cuda(), w.N, w.causal)
+    torch.cuda.synchronize()
+    rsa.check_device_error()
+    ro, rl = oracle.attention(q, k, v, w.causal)
+    assert_close(out, lse, ro, rl, torch.float32, what=w.name)
+
+
+def test_noncausal_bf16_workload_all_rows():
+    need_cuda()
+    w = rsa_inputs.WORKLOADS["noncausal_bf16"]
+    q, k, v = rsa_inputs.make_workload(w, seed=0, device="cpu")
+    out, lse = rsa.ring_attn(q.cuda(), k.cuda(), v.cuda(), w.N, w.causal)
+    torch.cuda.synchronize()
+    rsa.check_device_error()
+    ro, rl = oracle.attention(q, k, v, w.causal)
+    assert_close(out, lse, ro, rl, torch.bfloat16, what=w.name)
+
+
+RING_CASES = [
+    # B, H, T, d, N, causal, dtype
+    (1, 1, 1, 128, 1, True, torch.bfloat16),      # a single token
+    (1, 2, 127, 128, 1, True, torch.bfloat16),
+    (1, 2, 129, 128, 3, True, torch.bfloat16),    # chunks of 43
+    (2, 2, 384, 128, 3, False, torch.bfloat16),
+    (1, 3, 1000, 128, 8, True, torch.bfloat16),   # chunks of 125
+    (1, 2, 1024, 128, 4, True, torch.bfloat16),
+    (1, 1, 2048, 128, 16, True, torch.bfloat16),  # many small chunks
+    (1, 1, 96, 128, 96, True, torch.bfloat16),    # chunks of one token
+    (2, 2, 768, 64, 3, True, torch.bfloat16),     # d = 64
+    (1, 2, 300, 64, 5, False, torch.float32),
+    (1, 1, 200, 128, 4, True, torch.float32),
+]
+
+
+@pytest.mark.parametrize("case", RING_CASES, ids=lambda c: "B{}H{}T{}d{}N{}_{}_{}".format(
+    *c[:5], "causal" if c[5] else "full", "bf16" if c[6] == torch.bfloat16 else "f32"))
+def test_ring_matches_oracle(case):
+    need_cuda()
+    B, H, T, d, N, causal, dtype = case
+    (q, k, v), (qd, kd, vd) = qkv_cuda(B, H, T, d, dtype, seed=T + N)
+    out, lse = rsa.ring_attn(qd, kd, vd, N, causal)
+    torch.cuda.synchronize()
+    rsa.check_device_error()
+    ro, rl = oracle.attention(q, k, v, causal)
+    assert_close(out, lse, ro, rl, dtype, what=str(case))
+
+
+def test_ring_n1_and_n4_agree_and_row0_is_v0():
+    need_cuda()
+    B, H, T, d = 1, 4, 4096, 128
+    (q, k, v), (qd, kd, vd) = qkv_cuda(B, H, T, d, torch.bfloat16, seed=5)
+    o1, l1 = rsa.ring_attn(qd, kd, vd, 1, True)
+    o4, l4 = rsa.ring_attn(qd, kd, vd, 4, True)
+    torch.cuda.synchronize()
+    # row 0 sees only key 0: p = 1 exactly, so out[0] is V[0] to the bit
+    assert torch.equal(o1[:, :, 0], vd[:, :, 0])
+    assert torch.equal(o4[:, :, 0], vd[:, :, 0])
+    diff = (o1.float() - o4.float()).abs().max().item()
+    assert diff <= 2e-2
+    assert (l1 - l4).abs().max().item() <= 1e-3
+
+
+def test_chunk0_is_bit_identical_when_later_chunks_change():
+    # Causal: chunk 0 only ever meets its own KV chunk.
+    need_cuda()
+    B, H, T, d, N = 1, 2, 2048, 128, 4
+    (q, k, v), (qd, kd, vd) = qkv_cuda(B, H, T, d, torch.bfloat16, seed=6)
+    o_a, l_a = rsa.ring_attn(qd, kd, vd, N, True)
+    kd2, vd2 = kd.clone(), vd.clone()
+    Tc = T // N
+    kd2[:, :, Tc:] = torch.randn_like(kd2[:, :, Tc:].float()).to(torch.bfloat16)
+    vd2[:, :, Tc:] = torch.randn_like(vd2[:, :, Tc:].float()).to(torch.bfloat16)
+    o_b, l_b = rsa.ring_attn(qd, kd2, vd2, N, True)
+    torch.cuda.synchronize()
+    assert torch.equal(o_a[:, :, :Tc], o_b[:, :, :Tc])
+    assert torch.equal(l_a[:, :, :Tc], l_b[:, :, :Tc])
+    assert not torch.equal(o_a[:, :, Tc:], o_b[:, :, Tc:])
+
+
+def test_ring_is_deterministic():
+    need_cuda()
+    (q, k, v), (qd, kd, vd) = qkv_cuda(2, 2, 1024, 128, torch.bfloat16, seed=7)
+    a = rsa.ring_attn(qd, kd, vd, 4, True)
+    b = rsa.ring_attn(qd, kd, vd, 4, True)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_ring_outputs_leave_guard_bytes_alone():
+    need_cuda()
+    B, H, T, d, N = 1, 2, 1000, 128, 8
+    (q, k, v), (qd, kd, vd) = qkv_cuda(B, H, T, d, torch.bfloat16, seed=8)
+    pad = 8192
+    n_o = B * H * T * d
+    o_buf = torch.full((pad + n_o + pad,), 3.0, dtype=torch.bfloat16, device="cuda")
+    l_buf = torch.full((pad + B * H * T + pad,), 3.0, dtype=torch.float32, device="cuda")
+    need = rsa.workspace_size(torch.bfloat16, B, H, T, d, N, True)
+    ws_buf = torch.full((pad + need + pad,), 0x5a, dtype=torch.uint8, device="cuda")
+    out = o_buf[pad:pad + n_o].view(B, H, T, d)
+    lse = l_buf[pad:pad + B * H * T].view(B, H, T)
+    rsa.ring_attn(qd, kd, vd, N, True, out=out, lse=lse, workspace=ws_buf[pad:pad + need])
+    torch.cuda.synchronize()
+    assert torch.all(o_buf[:pad] == 3) and torch.all(o_buf[pad + n_o:] == 3)
+    assert torch.all(l_buf[:pad] == 3) and torch.all(l_buf[pad + B * H * T:] == 3)
+    assert torch.all(ws_buf[:pad] == 0x5a) and torch.all(ws_buf[pad + need:] == 0x5a)
+    ro, rl = oracle.attention(q, k, v, True)
+    assert_close(out, lse, ro, rl, torch.bfloat16)
+
+
+def test_timed_ring_records_every_launch():
+    need_cuda()
+    B, H, T, d, N = 1, 2, 1024, 128, 4
+    (q, k, v), (qd, kd, vd) = qkv_cuda(B, H, T, d, torch.bfloat16, seed=9)
+    n = rsa.ring_launch_count(N, True)
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    out = torch.empty_like(qd)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
+    ws = torch.empty(rsa.workspace_size(torch.bfloat16, B, H, T, d, N, True), dtype=torch.uint8, device="cuda")
+    kinds = rsa.ring_attn_timed(qd, kd, vd, N, True, out, lse, ws, ev0, ev1)
+    torch.cuda.synchronize()
+    assert kinds == [0] + [0, 1] * (N - 1)
+    assert all(a.elapsed_time(b) >= 0 for a, b in zip(ev0, ev1))
+    ro, rl = oracle.attention(q, k, v, True)
+    assert_close(out, lse, ro, rl, torch.bfloat16)
+
+
+def test_wait_limit_selftest_reports_timeout_and_context_survives():
+    need_cuda()
+    rsa.set_wait_limit_ns(50_000_000)
+    try:
+        rsa.selftest_wait_timeout()
+        with pytest.raises(rsa.RsaError) as ei:
+            rsa.check_device_error()
+        assert ei.value.status == 4
+    finally:
+        rsa.set_wait_limit_ns(2_000_000_000)
+    rsa.check_device_error()  # cleared
+    # the context still works
+    (q, k, v), (qd, kd, vd) = qkv_cuda(1, 1, 256, 128, torch.bfloat16, seed=10)
+    out, lse = rsa.ring_attn(qd, kd, vd, 2, True)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(q, k, v, True)
+    assert_close(out, lse, ro, rl, torch.bfloat16)
+
+
+def test_unsupported_and_invalid_calls_raise():
+    need_cuda()
+    q = torch.zeros(1, 1, 256, 96, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(rsa.RsaError):
+        rsa.ring_attn(q, q, q, 4, True)
+    q = torch.zeros(1, 1, 256, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(rsa.RsaError):
+        rsa.ring_attn(q, q, q, 3, True)

@@ -1,0 +1,133 @@
+"""Host-side checks of the C ABI: the library builds and loads, exports every
+symbol include/*.h declares, schedules the ring as the pages print it, sizes
+its workspace, and rejects bad arguments before touching a GPU.  No GPU."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import ROOT, read_golden
+
+import context_attention_rsa_gb300 as rsa
+
+FAKE = 0x10000  # a 16-byte-aligned non-null pointer value; never dereferenced
+
+
+def declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(rsa_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    lib = rsa.load()
+    names = declared_symbols()
+    assert "rsa_ring_attn_fwd" in names and "rsa_block_attn_fwd" in names and "rsa_merge" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert rsa.version() == 10000
+    assert lib.rsa_status_string(4) == b"RSA_ERR_TIMEOUT"
+
+
+def test_schedule_matches_printed_ring_table():
+    want = {}
+    for rnd1, gpu, kv in (map(int, r) for r in read_golden("ring_table_n4.txt")):
+        want.setdefault(rnd1 - 1, []).append((gpu, kv))
+    for r, pairs in want.items():
+        assert rsa.ring_schedule(4, False, r) == sorted(pairs)
+
+
+def test_schedule_causal_needs_and_counts():
+    for row in read_golden("causal_chunk_needs_n4.txt"):
+        i = int(row[0])
+        need = sorted(int(x) for x in row[1].split(","))
+        got = sorted(j for r in range(4) for (ii, j) in rsa.ring_schedule(4, True, r) if ii == i)
+        assert got == need
+    for N in (1, 2, 3, 4, 7, 16, 64):
+        pc = [p for r in range(N) for p in rsa.ring_schedule(N, True, r)]
+        pn = [p for r in range(N) for p in rsa.ring_schedule(N, False, r)]
+        assert len(pc) == N * (N + 1) // 2 and len(set(pc)) == len(pc)
+        assert len(pn) == N * N and len(set(pn)) == len(pn)
+        assert rsa.ring_schedule(N, True, 0) == [(i, i) for i in range(N)]
+
+
+def test_launch_count():
+    assert rsa.ring_launch_count(1, True) == 1
+    assert rsa.ring_launch_count(4, True) == 1 + 2 * 3
+    assert rsa.ring_launch_count(16, True) == 1 + 2 * 15
+    assert rsa.ring_launch_count(4, False) == 1 + 2 * 3
+
+
+def test_workspace_size():
+    import torch
+    B, H, T, d, N = 8, 64, 32768, 128, 4
+    ws = rsa.workspace_size(torch.bfloat16, B, H, T, d, N, True)
+    acc = B * H * T * d * 4
+    Tc = T // N
+    blk = (N - 1) * B * H * Tc * d * 2 + (N - 1) * B * H * Tc * 4
+    assert ws == acc + blk
+    assert rsa.workspace_size(torch.bfloat16, 1, 1, 256, 128, 1, True) == 0
+    # non-causal rounds have N pairs
+    ws2 = rsa.workspace_size(torch.float32, 1, 1, 256, 64, 4, False)
+    assert ws2 == 256 * 64 * 4 + 4 * 64 * 64 * 4 + 4 * 64 * 4
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(N=3), 1),           # N does not divide T
+    (dict(N=0), 1),
+    (dict(d=96), 2),          # unsupported head dim
+    (dict(T=0), 1),
+    (dict(dt=7), 1),
+])
+def test_ring_rejects_bad_shapes(kwargs, code):
+    lib = rsa.load()
+    a = dict(q=FAKE, k=FAKE, v=FAKE, dt=1, B=1, H=1, T=256, d=128, N=4, causal=1, out=FAKE, lse=FAKE,
+             ws=FAKE, ws_bytes=1 << 40, stream=None)
+    a.update(kwargs)
+    st = lib.rsa_ring_attn_fwd(a["q"], a["k"], a["v"], a["dt"], a["B"], a["H"], a["T"], a["d"], a["N"],
+                               a["causal"], a["out"], a["lse"], a["ws"], a["ws_bytes"], a["stream"])
+    assert st == code, lib.rsa_last_error_string()
+
+
+def test_ring_rejects_null_misaligned_and_small_workspace():
+    lib = rsa.load()
+    args = [FAKE, FAKE, FAKE, 1, 1, 1, 256, 128, 4, 1, FAKE, FAKE, FAKE, 1 << 40, None]
+    for idx in (0, 1, 2, 10, 11, 12):
+        bad = list(args)
+        bad[idx] = None
+        assert lib.rsa_ring_attn_fwd(*bad) == 1
+        bad[idx] = FAKE + 4
+        assert lib.rsa_ring_attn_fwd(*bad) == 1
+    small = list(args)
+    small[13] = 100
+    assert lib.rsa_ring_attn_fwd(*small) == 1
+    assert b"workspace" in lib.rsa_last_error_string()
+
+
+def test_block_rejects_pairs_outside_the_sequence():
+    lib = rsa.load()
+    base = [FAKE, FAKE, FAKE, 1, 1, 1, 256, 128]
+    for q_off, q_len, kv_off, kv_len in [(200, 100, 0, 10), (-1, 10, 0, 10), (0, 0, 0, 10),
+                                         (0, 10, 250, 7), (0, 10, 0, 0)]:
+        st = lib.rsa_block_attn_fwd(*base, q_off, q_len, kv_off, kv_len, 1, FAKE, FAKE, None)
+        assert st == 1
+
+
+def test_merge_rejects_bad_arguments():
+    lib = rsa.load()
+    assert lib.rsa_merge(FAKE, FAKE, FAKE, 1, FAKE, 0, 128, None) == 1
+    assert lib.rsa_merge(FAKE, FAKE, FAKE, 1, FAKE, 10, 96, None) == 2
+    assert lib.rsa_merge(None, FAKE, FAKE, 1, FAKE, 10, 128, None) == 1
+    assert lib.rsa_merge_finalize(FAKE, FAKE, FAKE, 1, FAKE, 10, 128, None, 1, FAKE, None) == 1
+
+
+def test_wait_limit_bounds():
+    lib = rsa.load()
+    assert lib.rsa_set_wait_limit_ns(10) == 1
+    assert lib.rsa_set_wait_limit_ns(2_000_000_000) == 0
