@@ -36,8 +36,10 @@ def useful_flops(B, H, T, d, causal):
 
 
 def merge_bytes_per_step(w, sched):
-    """Algorithmic merge bytes of one ring: 10d+12 per row per merge, 8d+12 for
-    a chunk's last (finalising) merge (bf16 partials, fp32 accumulator)."""
+    """Algorithmic merge bytes of one ring.  Per row and merge: read the fp32
+    accumulator (4d) and the fp32 partial (4d) and both lse values (8), write
+    the accumulator (4d) and its lse (4): 12d+12.  A chunk's last merge writes
+    the output in the input dtype instead: (8+esz)d+12."""
     BH = w.B * w.H
     Tc = w.T // w.N
     esz = 2 if w.dtype == "bf16" else 4
@@ -45,10 +47,7 @@ def merge_bytes_per_step(w, sched):
     for r in range(1, w.N):
         for (i, j) in sched(r):
             last = (i if w.causal else w.N - 1) == r
-            if last:
-                per = 4 * w.d + esz * w.d + esz * w.d + 12
-            else:
-                per = 4 * w.d + esz * w.d + 4 * w.d + 12
+            per = (8 + esz) * w.d + 12 if last else 12 * w.d + 12
             total += BH * Tc * per
     return total
 

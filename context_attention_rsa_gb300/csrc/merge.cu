@@ -11,8 +11,8 @@
 //
 // Layout: d/8 threads per row, each owning 8 consecutive columns, so a warp
 // reads whole rows with 16-byte vector accesses (two for fp32, one for bf16).
-// Streaming cache hints keep the one-touch data from displacing L2.
-// Grid-stride loop over rows of all pairs in the launch.
+// Streaming cache hints keep the one-touch data from displacing L2.  Each
+// (pair, head) segment is contiguous in memory, so indices need no division.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -23,6 +23,7 @@ namespace rsa {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kUnroll = 2;  // 8-column vectors per thread
 
 __device__ __forceinline__ void load8_f32(const float *p, float *x)
 {
@@ -61,83 +62,96 @@ __device__ __forceinline__ void store8_bf16(__nv_bfloat16 *p, const float *x)
            make_uint4(pack2(x[0], x[1]), pack2(x[2], x[3]), pack2(x[4], x[5]), pack2(x[6], x[7])));
 }
 
+// blockIdx.y walks the (pair, head) segments of the launch; inside a segment
+// the Tc rows are contiguous both in the accumulator and in the partial, so a
+// block covers kThreads * kUnroll consecutive 8-column vectors of one segment.
 __global__ void __launch_bounds__(kThreads)
-    merge_kernel(const __grid_constant__ MergeParams p)
+    merge_kernel(const __grid_constant__ MergeParams p, int log2_tpr)
 {
-    const int tpr = p.d >> 3;  // threads per row
-    const int64_t total = (int64_t)p.npairs * p.rows_per_pair * tpr;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += stride) {
-        const int64_t row = g / tpr;
-        const int col = (int)(g - row * tpr) * 8;
-        const int pi = (int)(row / p.rows_per_pair);
-        const int64_t rr = row - (int64_t)pi * p.rows_per_pair;
-        const int64_t bh = rr / p.Tc;
-        const int64_t t = rr - bh * p.Tc;
+    const int64_t BH = p.rows_per_pair / p.Tc;
+    const int64_t nseg = (int64_t)p.npairs * BH;
+    const int64_t nvec = p.Tc << log2_tpr;  // 8-column vectors per segment
+    const int tpr_mask = (1 << log2_tpr) - 1;
+    for (int64_t seg = blockIdx.y; seg < nseg; seg += gridDim.y) {
+        const int pi = (int)(seg / BH);
+        const int64_t bh = seg - (int64_t)pi * BH;
         const MergePair &mp = p.pairs[pi];
-        const int64_t arow = bh * p.T + mp.acc_t0 + t;
-
-        const float a = p.lse_acc[arow];
-        const float b = mp.lse_blk[rr];
-        const float M = fmaxf(a, b);
-        float wa = 0.f, wb = 0.f, L = -INFINITY;
-        if (M > -INFINITY) {
-            const float ea = __expf(a - M);
-            const float eb = __expf(b - M);
-            const float s = ea + eb;
-            const float inv = 1.f / s;
-            L = M + __logf(s);
-            wa = ea * inv;
-            wb = eb * inv;
-        }
-        float x[8], y[8];
-        load8_f32(p.o_acc + arow * p.d + col, x);
-        if (p.blk_f32)
-            load8_f32(static_cast<const float *>(mp.o_blk) + rr * p.d + col, y);
-        else
-            load8_bf16(static_cast<const __nv_bfloat16 *>(mp.o_blk) + rr * p.d + col, y);
+        const int64_t arow0 = bh * p.T + mp.acc_t0;  // first accumulator row of the segment
+        const int64_t brow0 = bh * p.Tc;             // first partial row of the segment
+        float a[kUnroll], b[kUnroll], x[kUnroll][8], y[kUnroll][8];
+        int64_t vv[kUnroll];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            x[i] = x[i] * wa + y[i] * wb;
-        // Every thread of the row has read lse_acc before one of them overwrites it.
-        __syncwarp(__activemask());
-        if (mp.final_) {
-            if (p.out_f32)
-                store8_f32(static_cast<float *>(p.out) + arow * p.d + col, x);
-            else
-                store8_bf16(static_cast<__nv_bfloat16 *>(p.out) + arow * p.d + col, x);
-            if (col == 0)
-                p.lse_out[arow] = L;
-        } else {
-            store8_f32(p.o_acc + arow * p.d + col, x);
-            if (col == 0)
-                p.lse_acc[arow] = L;
+        for (int u = 0; u < kUnroll; ++u) {
+            vv[u] = ((int64_t)blockIdx.x * kUnroll + u) * kThreads + threadIdx.x;
+            if (vv[u] < nvec) {
+                const int64_t r = vv[u] >> log2_tpr;
+                const int col = (int)(vv[u] & tpr_mask) * 8;
+                a[u] = p.lse_acc[arow0 + r];
+                b[u] = mp.lse_blk[brow0 + r];
+                load8_f32(p.o_acc + (arow0 + r) * p.d + col, x[u]);
+                if (p.blk_f32)
+                    load8_f32(static_cast<const float *>(mp.o_blk) + (brow0 + r) * p.d + col, y[u]);
+                else
+                    load8_bf16(static_cast<const __nv_bfloat16 *>(mp.o_blk) + (brow0 + r) * p.d + col, y[u]);
+            }
         }
+        // Every thread of a row has read lse_acc before one of them overwrites it.
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            if (vv[u] >= nvec)
+                continue;
+            const int64_t r = vv[u] >> log2_tpr;
+            const int col = (int)(vv[u] & tpr_mask) * 8;
+            const float M = fmaxf(a[u], b[u]);
+            float wa = 0.f, wb = 0.f, L = -INFINITY;
+            if (M > -INFINITY) {
+                const float ea = __expf(a[u] - M);
+                const float eb = __expf(b[u] - M);
+                const float sum = ea + eb;
+                const float inv = 1.f / sum;
+                L = M + __logf(sum);
+                wa = ea * inv;
+                wb = eb * inv;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                x[u][i] = x[u][i] * wa + y[u][i] * wb;
+            const int64_t arow = arow0 + r;
+            if (mp.final_) {
+                if (p.out_f32)
+                    store8_f32(static_cast<float *>(p.out) + arow * p.d + col, x[u]);
+                else
+                    store8_bf16(static_cast<__nv_bfloat16 *>(p.out) + arow * p.d + col, x[u]);
+                if (col == 0)
+                    p.lse_out[arow] = L;
+            } else {
+                store8_f32(p.o_acc + arow * p.d + col, x[u]);
+                if (col == 0)
+                    p.lse_acc[arow] = L;
+            }
+        }
+        __syncwarp();
     }
-}
-
-int sm_count()
-{
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-        return 148;
-    return n;
 }
 
 }  // namespace
 
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t s)
 {
-    const int64_t threads = (int64_t)p.npairs * p.rows_per_pair * (p.d >> 3);
-    if (threads <= 0)
+    if (p.npairs <= 0 || p.rows_per_pair <= 0 || p.Tc <= 0)
         return cudaSuccess;
-    static int sms = sm_count();
-    int64_t blocks = (threads + kThreads - 1) / kThreads;
-    const int64_t cap = (int64_t)sms * (2048 / kThreads);
-    if (blocks > cap)
-        blocks = cap;
-    merge_kernel<<<(unsigned)blocks, kThreads, 0, s>>>(p);
+    if (p.d != 64 && p.d != 128)
+        return cudaErrorInvalidValue;
+    const int log2_tpr = p.d == 128 ? 4 : 3;
+    const int64_t nvec = p.Tc << log2_tpr;
+    const int64_t per_block = (int64_t)kThreads * kUnroll;
+    const int64_t bx = (nvec + per_block - 1) / per_block;
+    const int64_t nseg = (int64_t)p.npairs * (p.rows_per_pair / p.Tc);
+    if (bx > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    dim3 grid((unsigned)bx, (unsigned)(nseg < 65535 ? nseg : 65535));
+    merge_kernel<<<grid, kThreads, 0, s>>>(p, log2_tpr);
     return cudaGetLastError();
 }
 

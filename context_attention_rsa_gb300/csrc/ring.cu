@@ -9,6 +9,9 @@
 // running-statistics rescale ("But softmax seems to require all attention
 // scores at once").
 //
+// Each round's partials are kept in fp32 in the workspace: a bf16 partial
+// would add a second rounding on top of the final bf16 output.
+//
 // Here every chunk is resident on the one GPU, so "sending a KV block to the
 // next GPU" becomes pointing the next round's pairs at another chunk's base
 // offset: no copy, no collective.  One block-attention launch covers all pairs
@@ -158,7 +161,8 @@ WsLayout ws_layout(rsa_dtype dt, int B, int H, int64_t T, int d, int N, int caus
     WsLayout w{};
     const size_t BH = (size_t)B * H;
     const size_t Tc = (size_t)(T / N);
-    const size_t esz = dt == RSA_BF16 ? 2 : 4;
+    const size_t esz = 4;  // partials stay fp32 whatever the input dtype
+    (void)dt;
     int maxp = 0;
     for (int r = 1; r < N; ++r) {
         const int np = round_pairs(N, causal, r, nullptr, nullptr);
@@ -279,7 +283,7 @@ rsa_status ring_run(const void *q, const void *k, const void *v, rsa_dtype dt, i
     causal = causal ? 1 : 0;
     const int64_t Tc = T / N;
     const int64_t BH = (int64_t)B * H;
-    const size_t esz = dt == RSA_BF16 ? 2 : 4;
+    const size_t esz = 4;  // fp32 partials
     char *wsb = static_cast<char *>(ws);
     float *o_acc = lay.acc ? reinterpret_cast<float *>(wsb) : nullptr;
     char *oblk = wsb + lay.acc;
@@ -314,7 +318,7 @@ rsa_status ring_run(const void *q, const void *k, const void *v, rsa_dtype dt, i
             m.Tc = Tc;
             m.T = T;
             m.d = d;
-            m.blk_f32 = dt == RSA_F32;
+            m.blk_f32 = 1;
             m.out_f32 = dt == RSA_F32;
             m.o_acc = o_acc;
             m.lse_acc = lse;
@@ -332,7 +336,7 @@ rsa_status ring_run(const void *q, const void *k, const void *v, rsa_dtype dt, i
                 pd.lse = lb;
                 pd.out_T = Tc;
                 pd.out_t0 = 0;
-                pd.out_f32 = dt == RSA_F32;
+                pd.out_f32 = 1;
                 MergePair &mp = m.pairs[m.npairs++];
                 mp.acc_t0 = i * Tc;
                 mp.o_blk = ob;

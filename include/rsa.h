@@ -106,8 +106,9 @@ rsa_status rsa_merge_finalize(const float *o_acc, const float *lse_acc, const vo
 
 /*
  * Bytes of device workspace rsa_ring_attn_fwd needs for this shape (written
- * to *bytes): an fp32 accumulator for the chunks visited more than once plus
- * room for one round's partial results.
+ * to *bytes): an fp32 accumulator [B, H, T, d] (none when N = 1) plus room
+ * for one round's partial results (fp32 o and lse of every pair in the
+ * largest round).
  */
 rsa_status rsa_ring_attn_workspace_size(rsa_dtype dt, int B, int H, int64_t T, int d, int N,
                                         int causal, size_t *bytes);

@@ -70,7 +70,7 @@ def test_workspace_size():
     ws = rsa.workspace_size(torch.bfloat16, B, H, T, d, N, True)
     acc = B * H * T * d * 4
     Tc = T // N
-    blk = (N - 1) * B * H * Tc * d * 2 + (N - 1) * B * H * Tc * 4
+    blk = (N - 1) * B * H * Tc * d * 4 + (N - 1) * B * H * Tc * 4  # fp32 partials
     assert ws == acc + blk
     assert rsa.workspace_size(torch.bfloat16, 1, 1, 256, 128, 1, True) == 0
     # non-causal rounds have N pairs
