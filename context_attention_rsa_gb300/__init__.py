@@ -24,7 +24,7 @@ from . import _build
 
 __all__ = [
     "RsaError", "load", "library_path", "block_attn_fwd", "merge", "merge_finalize",
-    "ring_attn", "ring_attn_timed", "ring_attn_from_host", "workspace_size", "ring_schedule",
+    "ring_attn", "ring_attn_noalloc", "ring_attn_timed", "ring_attn_from_host", "workspace_size", "ring_schedule",
     "set_wait_limit_ns", "check_device_error", "selftest_wait_timeout", "version",
     "RSA_F32", "RSA_BF16",
 ]
@@ -59,6 +59,8 @@ _SIGS = {
                                      ctypes.POINTER(ctypes.c_size_t)],
     "rsa_ring_attn_fwd": [_c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _i64, _i32, _i32, _i32,
                           _c_void_p, _c_void_p, _c_void_p, ctypes.c_size_t, _c_void_p],
+    "rsa_ring_attn_fwd_noalloc": [_c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _i64, _i32, _i32,
+                                  _i32, _c_void_p, _c_void_p, _c_void_p],
     "rsa_ring_attn_fwd_timed": [_c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _i64, _i32, _i32,
                                 _i32, _c_void_p, _c_void_p, _c_void_p, ctypes.c_size_t, _c_void_p,
                                 ctypes.POINTER(_c_void_p), ctypes.POINTER(_c_void_p),
@@ -201,6 +203,22 @@ def ring_attn(q, k, v, N: int, causal: bool, out=None, lse=None, workspace=None,
     _call("rsa_ring_attn_fwd", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
           int(bool(causal)), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
           workspace.numel() * workspace.element_size(), _stream(stream))
+    return out, lse
+
+
+def ring_attn_noalloc(q, k, v, N: int, causal: bool, out=None, lse=None,
+                      stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """ring_attn without a workspace, for callers that cannot allocate device
+    memory at call time: the library's built-in 64 MiB scratch array is used
+    instead (shapes needing more are rejected).  Calls share that array, so
+    calls that could overlap on the GPU must be serialised by the caller."""
+    B, H, T, d = _check_qkv(q, k, v)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    _call("rsa_ring_attn_fwd_noalloc", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
+          int(bool(causal)), out.data_ptr(), lse.data_ptr(), _stream(stream))
     return out, lse
 
 

@@ -130,6 +130,25 @@ rsa_status rsa_ring_attn_fwd(const void *q, const void *k, const void *v, rsa_dt
                              rsa_stream_t stream);
 
 /*
+ * rsa_ring_attn_fwd for callers that cannot allocate device memory (the pages
+ * have no counterpart; this is a library convenience).  Some callers cannot
+ * provide a workspace: their device memory belongs to another allocator that
+ * must not be bypassed, or a cudaMalloc (with the synchronisation it may
+ * imply) is not allowed where they run.  This call uses a fixed 64 MiB
+ * scratch array built into the library instead and allocates nothing.
+ * Arguments and results are those of rsa_ring_attn_fwd; a shape whose
+ * workspace (rsa_ring_attn_workspace_size) exceeds 64 MiB is rejected with
+ * RSA_ERR_INVALID_ARG.  Once used on a device, the 64 MiB stay reserved there
+ * until the process exits.  The first call on each device looks up the
+ * scratch address; make it before any stream capture.  All calls share the
+ * one scratch array, so calls that may overlap on the GPU (different streams
+ * or unsynchronised host threads) race and must be serialised by the caller.
+ */
+rsa_status rsa_ring_attn_fwd_noalloc(const void *q, const void *k, const void *v, rsa_dtype dt,
+                                     int B, int H, int64_t T, int d, int N, int causal,
+                                     void *out, float *lse, rsa_stream_t stream);
+
+/*
  * rsa_ring_attn_fwd with profiling: before and after each kernel launch it
  * records ev_start[i] / ev_stop[i] on `stream` and sets kind[i] to 0 for a
  * block-attention launch or 1 for a merge launch.  `cap` is the length of the
