@@ -73,6 +73,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Keep uses of r[0..31] after a preceding volatile asm (the TMEM load wait).
 __device__ __forceinline__ void tie32(uint32_t *r)
 {
@@ -104,13 +111,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
 
     // ---- which pair, head and 256-row group ------------------------------------
-    const int64_t BH = (int64_t)p.B * p.H;
-    const int64_t per_group = (int64_t)p.npairs * BH;
+    // All row groups of one (pair, head) are consecutive blocks, so the CTAs
+    // running at the same time stream the same K/V chunk and share it in L2.
+    // Inside a (pair, head) the heaviest causal groups come first.
     const int64_t L = blockIdx.x;
-    const int qg = p.n_qgroups - 1 - (int)(L / per_group);  // heaviest causal groups first
-    const int64_t rest = L % per_group;
-    const int pi = (int)(rest / BH);
-    const int bh = (int)(rest % BH);
+    const int64_t unit = L / p.n_qgroups;
+    const int qg = p.n_qgroups - 1 - (int)(L - unit * p.n_qgroups);
+    const int pi = (int)(unit % p.npairs);
+    const int bh = (int)(unit / p.npairs);
     const PairDesc &pr = p.pairs[pi];
     const int64_t q0 = (int64_t)qg * kBf16RowsPerCta;
     const int64_t rows_valid = min((int64_t)kBf16RowsPerCta, p.q_len - q0);
@@ -295,19 +303,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             tie32(s + 64);
             tie32(s + 96);
             const int64_t lim = allowed - (int64_t)j * 128;
-            float mx = -INFINITY;
-            if (lim >= 128) {
+            if (lim < 128) {
 #pragma unroll
                 for (int i = 0; i < 128; ++i)
-                    mx = fmaxf(mx, u2f(s[i]));
-            } else {
-#pragma unroll
-                for (int i = 0; i < 128; ++i) {
                     if ((int64_t)i >= lim)
                         s[i] = f2u(-INFINITY);
-                    mx = fmaxf(mx, u2f(s[i]));
-                }
             }
+            // row max: four independent chains of three-input max
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int i = 0; i < 128; i += 8) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    m4[c] = fmax3(m4[c], u2f(s[i + 2 * c]), u2f(s[i + 2 * c + 1]));
+            }
+            const float mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
             const float mnew = mx * sl2;
             const bool need = (mnew > -INFINITY) && (m_used == -INFINITY || mnew > m_used + kRescaleThreshold);
             if (__any_sync(0xffffffffu, need)) {
@@ -318,32 +328,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m_used = mnew;
                 }
                 if (j > 0) {
+                    const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t o[32];
                         ptx::tmem_ld32(tO + c * 32, o);
                         ptx::tmem_ld_wait(o);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            o[i] = f2u(u2f(o[i]) * alpha);
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 r = __fmul2_rn(make_float2(u2f(o[i]), u2f(o[i + 1])), a2);
+                            o[i] = f2u(r.x);
+                            o[i + 1] = f2u(r.y);
+                        }
                         ptx::tmem_st32(tO + c * 32, o);
                     }
                     ptx::tmem_st_wait();
                 }
             }
+            // p = 2^(s * log2(e)/sqrt(d) - m), written back over S as bf16 pairs
             const float neg = (m_used == -INFINITY) ? 0.f : -m_used;
-            float sum = 0.f;
-            uint32_t pk[64];
+            const float2 c2 = make_float2(sl2, sl2);
+            const float2 n2 = make_float2(neg, neg);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const float p0 = ptx::ex2(fmaf(u2f(s[2 * i]), sl2, neg));
-                const float p1 = ptx::ex2(fmaf(u2f(s[2 * i + 1]), sl2, neg));
-                sum += p0 + p1;
-                pk[i] = pack_bf16(p0, p1);
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int e = half * 64 + 2 * i;
+                    const float2 x = __ffma2_rn(make_float2(u2f(s[e]), u2f(s[e + 1])), c2, n2);
+                    const float p0 = ptx::ex2(x.x);
+                    const float p1 = ptx::ex2(x.y);
+                    acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
+                    pk[i] = pack_bf16(p0, p1);
+                }
+                ptx::tmem_st32(tS + half * 32, pk);
             }
-            l += sum;
-            ptx::tmem_st32(tS, pk);
-            ptx::tmem_st32(tS + 32, pk + 32);
+            const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+            const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+            const float2 a = __fadd2_rn(a01, a23);
+            l += a.x + a.y;
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
             ptx::mbar_arrive(BAR(C::kPF + t));
