@@ -191,6 +191,7 @@ def main():
     ap.add_argument("--workload", default="page1_causal_bf16")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fused", action="store_true", help="skip timing the fused-merge ring variant")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--shape", default=None,
                     help="B,H,T,d,N,causal: a bf16 normal-recipe workload instead of --workload (profiling)")
@@ -276,6 +277,32 @@ def main():
     mbytes = merge_bytes_per_step(w, lambda r: rsa.ring_schedule(N, causal, r))
     mrg_gbs = mbytes / (mrg_ms * 1e-3) / 1e9 if mrg_ms > 0 else None
 
+    # ---- the fused-merge ring (each pair's epilogue folds into the accumulator)
+    f1 = None
+    if not args.no_fused:
+        ws_f = torch.empty(max(rsa.workspace_size(q.dtype, B, H, T, d, N, causal, fused=True), 1),
+                           dtype=torch.uint8, device=dev)
+        n_f = rsa.ring_launch_count(N, causal, fused=True)
+        for _ in range(max(args.warmup, 0)):
+            rsa.ring_attn(q, k, v, N, causal, out=out, lse=lse, workspace=ws_f, fused=True)
+        fe0 = [[torch.cuda.Event(enable_timing=True) for _ in range(n_f)] for _ in range(args.steps)]
+        fe1 = [[torch.cuda.Event(enable_timing=True) for _ in range(n_f)] for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for s_ in range(args.steps):
+            rsa.ring_attn_timed(q, k, v, N, causal, out, lse, ws_f, fe0[s_], fe1[s_], fused=True)
+        t_stop.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        rsa.check_device_error()
+        f_ms = t_start.elapsed_time(t_stop) / args.steps
+        f_blk = sum(fe0[s_][i].elapsed_time(fe1[s_][i]) for s_ in range(args.steps) for i in range(n_f)) / args.steps
+        f1 = {"value": flops * world / (f_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": f_ms,
+              "block_kernel_tflops": flops / (f_blk * 1e-3) / 1e12, "launches_per_step": n_f,
+              "workspace_bytes": int(ws_f.numel())}
+        del ws_f
+
     # ---- end to end from pinned host memory (public API) --------------------
     e2e = None
     if args.e2e_steps > 0:
@@ -337,6 +364,7 @@ def main():
                       "frac": (mrg_gbs / peaks["hbm_gbs"]) if mrg_gbs else None,
                       "algorithmic_bytes_per_step": mbytes, "launches_per_step": n_mrg, "ms_per_step": mrg_ms,
                       "peak_source": peaks["source"] + " hbm_gbs"},
+            "fused_merge_ring": f1,
             "e2e": e2e,
             "gpu_launches": n_launch * args.steps,
             "cpu_baseline": cpu,

@@ -65,6 +65,12 @@ _SIGS = {
                                 _i32, _c_void_p, _c_void_p, _c_void_p, ctypes.c_size_t, _c_void_p,
                                 ctypes.POINTER(_c_void_p), ctypes.POINTER(_c_void_p),
                                 ctypes.POINTER(_i32), _i32, ctypes.POINTER(_i32)],
+    "rsa_ring_attn_workspace_size_ex": [_i32, _i32, _i32, _i64, _i32, _i32, _i32, ctypes.c_uint,
+                                        ctypes.POINTER(ctypes.c_size_t)],
+    "rsa_ring_attn_fwd_ex": [_c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _i64, _i32, _i32, _i32,
+                             ctypes.c_uint, _c_void_p, _c_void_p, _c_void_p, ctypes.c_size_t, _c_void_p,
+                             ctypes.POINTER(_c_void_p), ctypes.POINTER(_c_void_p), ctypes.POINTER(_i32),
+                             _i32, ctypes.POINTER(_i32)],
     "rsa_ring_schedule": [_i32, _i32, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _i32,
                           ctypes.POINTER(_i32)],
     "rsa_set_wait_limit_ns": [ctypes.c_uint64],
@@ -136,10 +142,18 @@ def _check_qkv(q, k, v) -> Tuple[int, int, int, int]:
     return B, H, T, d
 
 
-def workspace_size(dtype: torch.dtype, B: int, H: int, T: int, d: int, N: int, causal: bool) -> int:
+RSA_RING_FUSED_MERGE = 1
+
+
+def workspace_size(dtype: torch.dtype, B: int, H: int, T: int, d: int, N: int, causal: bool,
+                   fused: bool = False) -> int:
     n = ctypes.c_size_t(0)
     dt = RSA_F32 if dtype == torch.float32 else RSA_BF16
-    _call("rsa_ring_attn_workspace_size", dt, B, H, T, d, N, int(bool(causal)), ctypes.byref(n))
+    if fused:
+        _call("rsa_ring_attn_workspace_size_ex", dt, B, H, T, d, N, int(bool(causal)), RSA_RING_FUSED_MERGE,
+              ctypes.byref(n))
+    else:
+        _call("rsa_ring_attn_workspace_size", dt, B, H, T, d, N, int(bool(causal)), ctypes.byref(n))
     return int(n.value)
 
 
@@ -190,19 +204,26 @@ def merge_finalize(o_acc, lse_acc, o_blk, lse_blk, out_dtype=torch.bfloat16, out
 
 
 def ring_attn(q, k, v, N: int, causal: bool, out=None, lse=None, workspace=None,
-              stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """The whole ring: (out [B, H, T, d] in q's dtype, lse [B, H, T] fp32)."""
+              stream=None, fused: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The whole ring: (out [B, H, T, d] in q's dtype, lse [B, H, T] fp32).
+    fused=True folds each pair into the accumulator in the block epilogue
+    (RSA_RING_FUSED_MERGE) instead of launching the merge kernel."""
     B, H, T, d = _check_qkv(q, k, v)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
-    need = workspace_size(q.dtype, B, H, T, d, N, causal)
+    need = workspace_size(q.dtype, B, H, T, d, N, causal, fused)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    _call("rsa_ring_attn_fwd", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
-          int(bool(causal)), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
-          workspace.numel() * workspace.element_size(), _stream(stream))
+    if fused:
+        _call("rsa_ring_attn_fwd_ex", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
+              int(bool(causal)), RSA_RING_FUSED_MERGE, out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+              workspace.numel() * workspace.element_size(), _stream(stream), None, None, None, 0, None)
+    else:
+        _call("rsa_ring_attn_fwd", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
+              int(bool(causal)), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+              workspace.numel() * workspace.element_size(), _stream(stream))
     return out, lse
 
 
@@ -223,7 +244,7 @@ def ring_attn_noalloc(q, k, v, N: int, causal: bool, out=None, lse=None,
 
 
 def ring_attn_timed(q, k, v, N: int, causal: bool, out, lse, workspace, events_start: Sequence,
-                    events_stop: Sequence, stream=None) -> List[int]:
+                    events_stop: Sequence, stream=None, fused: bool = False) -> List[int]:
     """ring_attn that records the given torch.cuda.Event pairs around each
     kernel launch; returns the launch kinds (0 block attention, 1 merge)."""
     B, H, T, d = _check_qkv(q, k, v)
@@ -236,20 +257,26 @@ def ring_attn_timed(q, k, v, N: int, causal: bool, out, lse, workspace, events_s
     ev_e = (ctypes.c_void_p * cap)(*[int(e.cuda_event) for e in events_stop])
     kinds = (ctypes.c_int * cap)()
     n = ctypes.c_int(0)
-    _call("rsa_ring_attn_fwd_timed", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
-          int(bool(causal)), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
-          workspace.numel() * workspace.element_size(), _stream(stream), ev_s, ev_e, kinds, cap,
-          ctypes.byref(n))
+    if fused:
+        _call("rsa_ring_attn_fwd_ex", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
+              int(bool(causal)), RSA_RING_FUSED_MERGE, out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+              workspace.numel() * workspace.element_size(), _stream(stream), ev_s, ev_e, kinds, cap,
+              ctypes.byref(n))
+    else:
+        _call("rsa_ring_attn_fwd_timed", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
+              int(bool(causal)), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+              workspace.numel() * workspace.element_size(), _stream(stream), ev_s, ev_e, kinds, cap,
+              ctypes.byref(n))
     return [kinds[i] for i in range(n.value)]
 
 
-def ring_launch_count(N: int, causal: bool) -> int:
+def ring_launch_count(N: int, causal: bool, fused: bool = False) -> int:
     """Kernel launches one ring makes (block-attention plus merge launches)."""
     n = 0
     for r in range(N):
         np_ = len(ring_schedule(N, causal, r))
         groups = (np_ + 31) // 32
-        n += groups if r == 0 else 2 * groups
+        n += groups if (r == 0 or fused) else 2 * groups
     return n
 
 

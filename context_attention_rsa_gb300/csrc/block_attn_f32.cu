@@ -108,13 +108,30 @@ __global__ void __launch_bounds__(kWarps * 32)
 
     const int64_t orow = (int64_t)bh * pr.out_T + pr.out_t0 + r;
     const bool empty = !(l > 0.f);
-    const float inv = empty ? 0.f : 1.f / l;
+    const float lse_b = empty ? -INFINITY : m + logf(l);
+    float wa = 0.f, wb = empty ? 0.f : 1.f / l, lse_out = lse_b;
+    if (pr.mode != kStore) {
+        // fold into the running (acc, lse): M = max(a, b), L = M + ln(e^{a-M} + e^{b-M})
+        const float a = pr.lse[orow];
+        const float M = fmaxf(a, lse_b);
+        if (M > -INFINITY) {
+            const float ea = expf(a - M), eb = expf(lse_b - M);
+            lse_out = M + logf(ea + eb);
+            wa = ea / (ea + eb);
+            wb = empty ? 0.f : eb / (ea + eb) / l;
+        } else {
+            lse_out = -INFINITY;
+            wb = 0.f;
+        }
+    }
     float *out = static_cast<float *>(pr.out) + orow * D;
+    const float *acc = pr.acc + orow * D;
 #pragma unroll
     for (int i = 0; i < PER; ++i)
-        out[lane + 32 * i] = o[i] * inv;
+        out[lane + 32 * i] = pr.mode != kStore ? fmaf(o[i], wb, acc[lane + 32 * i] * wa) : o[i] * wb;
+    __syncwarp();  // every lane has read lse[orow] before lane 0 replaces it
     if (lane == 0)
-        pr.lse[orow] = empty ? -INFINITY : m + logf(l);
+        pr.lse[orow] = lse_out;
 }
 
 }  // namespace

@@ -379,12 +379,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
             ptx::tc_fence_after();
+            // This pair's result is (O / l, lse_b).  A merging epilogue folds it
+            // into the running (acc, lse) as the merge kernel does:
+            // M = max(a, b), L = M + ln(e^{a-M} + e^{b-M}), o = acc e^{a-L} + o_b e^{b-L}.
             const bool empty = !(l > 0.f);
-            const float inv = empty ? 0.f : 1.f / l;
             const bool valid = rg < p.q_len;
             const int64_t orow = (int64_t)bh * pr.out_T + pr.out_t0 + rg;
+            const float lse_b = empty ? -INFINITY : (m_used + ptx::lg2(l)) * 0.69314718055994531f;
+            float wa = 0.f;                           // weight of the accumulator row
+            float wb = empty ? 0.f : 1.f / l;         // weight of the unnormalised O row
+            float lse_out = lse_b;
+            const bool merging = pr.mode != kStore;
+            if (merging && valid) {
+                const float a = pr.lse[orow];
+                const float M = fmaxf(a, lse_b);
+                if (M > -INFINITY) {
+                    const float ea = ptx::ex2((a - M) * 1.4426950408889634f);
+                    const float eb = ptx::ex2((lse_b - M) * 1.4426950408889634f);
+                    const float tot = ea + eb;
+                    const float inv = 1.f / tot;
+                    lse_out = M + ptx::lg2(tot) * 0.69314718055994531f;
+                    wa = ea * inv;
+                    wb = empty ? 0.f : eb * inv / l;
+                } else {
+                    lse_out = -INFINITY;
+                    wb = 0.f;
+                }
+            }
             if (valid)
-                pr.lse[orow] = empty ? -INFINITY : (m_used + ptx::lg2(l)) * 0.69314718055994531f;
+                pr.lse[orow] = lse_out;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -397,20 +420,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                         o[i] = 0u;
                 }
                 if (valid) {
+                    float v[32];
+                    if (merging) {
+                        const float4 *src = reinterpret_cast<const float4 *>(pr.acc + orow * D + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 x = src[i];
+                            v[4 * i] = fmaf(u2f(o[4 * i]), wb, x.x * wa);
+                            v[4 * i + 1] = fmaf(u2f(o[4 * i + 1]), wb, x.y * wa);
+                            v[4 * i + 2] = fmaf(u2f(o[4 * i + 2]), wb, x.z * wa);
+                            v[4 * i + 3] = fmaf(u2f(o[4 * i + 3]), wb, x.w * wa);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = u2f(o[i]) * wb;
+                    }
                     if (pr.out_f32) {
                         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(pr.out) + orow * D + c * 32);
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            dst[i] = make_float4(u2f(o[4 * i]) * inv, u2f(o[4 * i + 1]) * inv,
-                                                 u2f(o[4 * i + 2]) * inv, u2f(o[4 * i + 3]) * inv);
+                            dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                     } else {
                         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.out) + orow * D + c * 32);
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
-                            dst[i] = make_uint4(pack_bf16(u2f(o[8 * i]) * inv, u2f(o[8 * i + 1]) * inv),
-                                                pack_bf16(u2f(o[8 * i + 2]) * inv, u2f(o[8 * i + 3]) * inv),
-                                                pack_bf16(u2f(o[8 * i + 4]) * inv, u2f(o[8 * i + 5]) * inv),
-                                                pack_bf16(u2f(o[8 * i + 6]) * inv, u2f(o[8 * i + 7]) * inv));
+                            dst[i] = make_uint4(pack_bf16(v[8 * i], v[8 * i + 1]), pack_bf16(v[8 * i + 2], v[8 * i + 3]),
+                                                pack_bf16(v[8 * i + 4], v[8 * i + 5]),
+                                                pack_bf16(v[8 * i + 6], v[8 * i + 7]));
                     }
                 }
             }

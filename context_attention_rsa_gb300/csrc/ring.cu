@@ -156,7 +156,7 @@ struct WsLayout {
     int maxp;
 };
 
-WsLayout ws_layout(rsa_dtype dt, int B, int H, int64_t T, int d, int N, int causal)
+WsLayout ws_layout(rsa_dtype dt, int B, int H, int64_t T, int d, int N, int causal, bool fused)
 {
     WsLayout w{};
     const size_t BH = (size_t)B * H;
@@ -168,6 +168,8 @@ WsLayout ws_layout(rsa_dtype dt, int B, int H, int64_t T, int d, int N, int caus
         const int np = round_pairs(N, causal, r, nullptr, nullptr);
         maxp = np > maxp ? np : maxp;
     }
+    if (fused)
+        maxp = 0;  // partials go straight into the accumulator
     w.maxp = maxp;
     w.acc = N > 1 ? align256(BH * (size_t)T * d * 4) : 0;
     w.oblk = align256((size_t)maxp * BH * Tc * d * esz);
@@ -176,12 +178,12 @@ WsLayout ws_layout(rsa_dtype dt, int B, int H, int64_t T, int d, int N, int caus
     return w;
 }
 
-int launch_count(int N, int causal)
+int launch_count(int N, int causal, bool fused)
 {
     int n = (N + kMaxPairsPerLaunch - 1) / kMaxPairsPerLaunch;
     for (int r = 1; r < N; ++r) {
         const int np = round_pairs(N, causal, r, nullptr, nullptr);
-        n += 2 * ((np + kMaxPairsPerLaunch - 1) / kMaxPairsPerLaunch);
+        n += (fused ? 1 : 2) * ((np + kMaxPairsPerLaunch - 1) / kMaxPairsPerLaunch);
     }
     return n;
 }
@@ -253,7 +255,7 @@ BlockParams base_params(rsa_dtype dt, int B, int H, int64_t T, int d, int causal
 
 rsa_status validate_ring(const void *q, const void *k, const void *v, rsa_dtype dt, int B, int H, int64_t T,
                          int d, int N, void *out, float *lse, void *ws, size_t ws_bytes, int causal,
-                         WsLayout *lay)
+                         bool fused, WsLayout *lay)
 {
     RSA_TRY(check_shape(dt, B, H, T, d));
     RSA_TRY(check_ptr(q, "q"));
@@ -265,7 +267,7 @@ rsa_status validate_ring(const void *q, const void *k, const void *v, rsa_dtype 
         return fail(RSA_ERR_INVALID_ARG, "N=%d must be >= 1 and divide T=%lld", N, (long long)T);
     if (N > 1024)
         return fail(RSA_ERR_UNSUPPORTED, "N=%d exceeds 1024 chunks", N);
-    *lay = ws_layout(dt, B, H, T, d, N, causal);
+    *lay = ws_layout(dt, B, H, T, d, N, causal, fused);
     if (lay->total > 0) {
         RSA_TRY(check_ptr(ws, "workspace"));
         if (ws_bytes < lay->total)
@@ -275,8 +277,8 @@ rsa_status validate_ring(const void *q, const void *k, const void *v, rsa_dtype 
 }
 
 rsa_status ring_run(const void *q, const void *k, const void *v, rsa_dtype dt, int B, int H, int64_t T, int d,
-                    int N, int causal, void *out, float *lse, void *ws, const WsLayout &lay, cudaStream_t s,
-                    Recorder *rec)
+                    int N, int causal, void *out, float *lse, void *ws, const WsLayout &lay, bool fused,
+                    cudaStream_t s, Recorder *rec)
 {
     unsigned int *err = nullptr;
     RSA_TRY(device_error_word(&err));
@@ -305,10 +307,32 @@ rsa_status ring_run(const void *q, const void *k, const void *v, rsa_dtype dt, i
         }
         RSA_TRY(launch_block(q, k, v, dt, p, s, rec));
     }
-    // Rounds 1..N-1: partials into the workspace, then merge.
+    // Rounds 1..N-1: partials into the workspace, then merge -- or, fused,
+    // each pair's epilogue folds its result into the accumulator directly.
     int qi[1024], kj[1024];
     for (int r = 1; r < N; ++r) {
         const int np = round_pairs(N, causal, r, qi, kj);
+        if (fused) {
+            for (int g0 = 0; g0 < np; g0 += kMaxPairsPerLaunch) {
+                BlockParams p = base_params(dt, B, H, T, d, causal, Tc, Tc, err);
+                for (int x = g0; x < np && p.npairs < kMaxPairsPerLaunch; ++x) {
+                    const int i = qi[x], j = kj[x];
+                    const bool last = r == visits(N, causal, i) - 1;
+                    PairDesc &pd = p.pairs[p.npairs++];
+                    pd.q_off = i * Tc;
+                    pd.kv_off = j * Tc;
+                    pd.out = last ? out : static_cast<void *>(o_acc);
+                    pd.lse = lse;
+                    pd.out_T = T;
+                    pd.out_t0 = i * Tc;
+                    pd.out_f32 = last ? (dt == RSA_F32) : 1;
+                    pd.mode = last ? kMergeFinal : kMergeAcc;
+                    pd.acc = o_acc;
+                }
+                RSA_TRY(launch_block(q, k, v, dt, p, s, rec));
+            }
+            continue;
+        }
         for (int g0 = 0; g0 < np; g0 += kMaxPairsPerLaunch) {
             const int gn = np - g0 < kMaxPairsPerLaunch ? np - g0 : kMaxPairsPerLaunch;
             BlockParams p = base_params(dt, B, H, T, d, causal, Tc, Tc, err);
@@ -441,7 +465,7 @@ rsa_status rsa_ring_attn_workspace_size(rsa_dtype dt, int B, int H, int64_t T, i
     RSA_TRY(check_shape(dt, B, H, T, d));
     if (N < 1 || N > T || T % N != 0)
         return fail(RSA_ERR_INVALID_ARG, "N=%d must be >= 1 and divide T=%lld", N, (long long)T);
-    *bytes = ws_layout(dt, B, H, T, d, N, causal).total;
+    *bytes = ws_layout(dt, B, H, T, d, N, causal, false).total;
     return RSA_OK;
 }
 
@@ -450,8 +474,38 @@ rsa_status rsa_ring_attn_fwd(const void *q, const void *k, const void *v, rsa_dt
                              rsa_stream_t stream)
 {
     WsLayout lay;
-    RSA_TRY(validate_ring(q, k, v, dt, B, H, T, d, N, out, lse, workspace, ws_bytes, causal, &lay));
-    return ring_run(q, k, v, dt, B, H, T, d, N, causal, out, lse, workspace, lay, stream, nullptr);
+    RSA_TRY(validate_ring(q, k, v, dt, B, H, T, d, N, out, lse, workspace, ws_bytes, causal, false, &lay));
+    return ring_run(q, k, v, dt, B, H, T, d, N, causal, out, lse, workspace, lay, false, stream, nullptr);
+}
+
+static rsa_status ring_profiled(const void *q, const void *k, const void *v, rsa_dtype dt, int B, int H,
+                                int64_t T, int d, int N, int causal, unsigned flags, void *out, float *lse,
+                                void *workspace, size_t ws_bytes, rsa_stream_t stream, rsa_event_t *ev_start,
+                                rsa_event_t *ev_stop, int *kind, int cap, int *n_launches)
+{
+    if (flags & ~(unsigned)RSA_RING_FUSED_MERGE)
+        return fail(RSA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    const bool fused = (flags & RSA_RING_FUSED_MERGE) != 0;
+    WsLayout lay;
+    RSA_TRY(validate_ring(q, k, v, dt, B, H, T, d, N, out, lse, workspace, ws_bytes, causal, fused, &lay));
+    const bool timed = ev_start || ev_stop || kind;
+    if (timed && (!ev_start || !ev_stop || !kind))
+        return fail(RSA_ERR_INVALID_ARG, "event and kind arrays must be given together");
+    const int need = launch_count(N, causal, fused);
+    if (n_launches)
+        *n_launches = need;
+    if (!timed)
+        return ring_run(q, k, v, dt, B, H, T, d, N, causal, out, lse, workspace, lay, fused, stream, nullptr);
+    if (cap < need)
+        return fail(RSA_ERR_INVALID_ARG, "cap=%d but the ring makes %d launches", cap, need);
+    Recorder rec;
+    rec.start = ev_start;
+    rec.stop = ev_stop;
+    rec.kind = kind;
+    rsa_status st = ring_run(q, k, v, dt, B, H, T, d, N, causal, out, lse, workspace, lay, fused, stream, &rec);
+    if (n_launches)
+        *n_launches = rec.n;
+    return st;
 }
 
 rsa_status rsa_ring_attn_fwd_timed(const void *q, const void *k, const void *v, rsa_dtype dt, int B, int H,
@@ -459,21 +513,33 @@ rsa_status rsa_ring_attn_fwd_timed(const void *q, const void *k, const void *v, 
                                    size_t ws_bytes, rsa_stream_t stream, rsa_event_t *ev_start,
                                    rsa_event_t *ev_stop, int *kind, int cap, int *n_launches)
 {
-    WsLayout lay;
-    RSA_TRY(validate_ring(q, k, v, dt, B, H, T, d, N, out, lse, workspace, ws_bytes, causal, &lay));
     if (!ev_start || !ev_stop || !kind || !n_launches)
         return fail(RSA_ERR_INVALID_ARG, "event/kind/count arrays must not be NULL");
-    const int need = launch_count(N, causal);
-    *n_launches = need;
-    if (cap < need)
-        return fail(RSA_ERR_INVALID_ARG, "cap=%d but the ring makes %d launches", cap, need);
-    Recorder rec;
-    rec.start = ev_start;
-    rec.stop = ev_stop;
-    rec.kind = kind;
-    rsa_status st = ring_run(q, k, v, dt, B, H, T, d, N, causal, out, lse, workspace, lay, stream, &rec);
-    *n_launches = rec.n;
-    return st;
+    return ring_profiled(q, k, v, dt, B, H, T, d, N, causal, 0u, out, lse, workspace, ws_bytes, stream, ev_start,
+                         ev_stop, kind, cap, n_launches);
+}
+
+rsa_status rsa_ring_attn_workspace_size_ex(rsa_dtype dt, int B, int H, int64_t T, int d, int N, int causal,
+                                           unsigned flags, size_t *bytes)
+{
+    if (!bytes)
+        return fail(RSA_ERR_INVALID_ARG, "bytes is NULL");
+    if (flags & ~(unsigned)RSA_RING_FUSED_MERGE)
+        return fail(RSA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    RSA_TRY(check_shape(dt, B, H, T, d));
+    if (N < 1 || N > T || T % N != 0)
+        return fail(RSA_ERR_INVALID_ARG, "N=%d must be >= 1 and divide T=%lld", N, (long long)T);
+    *bytes = ws_layout(dt, B, H, T, d, N, causal, (flags & RSA_RING_FUSED_MERGE) != 0).total;
+    return RSA_OK;
+}
+
+rsa_status rsa_ring_attn_fwd_ex(const void *q, const void *k, const void *v, rsa_dtype dt, int B, int H,
+                                int64_t T, int d, int N, int causal, unsigned flags, void *out, float *lse,
+                                void *workspace, size_t ws_bytes, rsa_stream_t stream, rsa_event_t *ev_start,
+                                rsa_event_t *ev_stop, int *kind, int cap, int *n_launches)
+{
+    return ring_profiled(q, k, v, dt, B, H, T, d, N, causal, flags, out, lse, workspace, ws_bytes, stream,
+                         ev_start, ev_stop, kind, cap, n_launches);
 }
 
 rsa_status rsa_ring_schedule(int N, int causal, int round, int *q_chunk, int *kv_chunk, int cap, int *n_pairs)

@@ -17,9 +17,17 @@ constexpr unsigned int kDevErrTimeout = 0x100u;
 // Most pairs one kernel launch takes; longer pair lists are split.
 constexpr int kMaxPairsPerLaunch = 32;
 
+// What a block-attention epilogue does with a pair's (o, lse).
+enum EpilogueMode : int {
+    kStore = 0,       // write (o, lse) to out/lse
+    kMergeAcc = 1,    // fold into the fp32 accumulator in place: acc/lse <- merge(acc/lse, o/lse)
+    kMergeFinal = 2,  // fold with the accumulator and write the result to out/lse (acc read only)
+};
+
 // One (query chunk, KV chunk) pair inside a block-attention launch.  Output
 // row r of head bh goes to out[(bh * out_T + out_t0 + r) * d] and
-// lse[bh * out_T + out_t0 + r].
+// lse[bh * out_T + out_t0 + r]; a merging epilogue reads the accumulator row
+// at the same index of `acc` (and the running lse from `lse`).
 struct PairDesc {
     int64_t q_off;   // global position of the first query row
     int64_t kv_off;  // global position of the first key
@@ -28,7 +36,8 @@ struct PairDesc {
     int64_t out_T;   // row pitch of out/lse per head
     int64_t out_t0;  // first row of this pair inside each head
     int out_f32;     // 1: fp32 output, 0: bf16 output
-    int pad_;
+    int mode;        // EpilogueMode
+    const float *acc;  // fp32 accumulator (kMergeAcc: same as out; kMergeFinal: read only)
 };
 
 struct BlockParams {

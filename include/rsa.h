@@ -163,6 +163,35 @@ rsa_status rsa_ring_attn_fwd_timed(const void *q, const void *k, const void *v, 
                                    rsa_event_t *ev_stop, int *kind, int cap, int *n_launches);
 
 /*
+ * Ring variant flags for rsa_ring_attn_fwd_ex / rsa_ring_attn_workspace_size_ex.
+ *
+ * RSA_RING_FUSED_MERGE: rounds after the first do not write partials; each
+ * pair's block epilogue folds its (o, lse) straight into the fp32 accumulator
+ * with the same merge rule as rsa_merge (and the chunk's last pair writes
+ * out/lse).  No merge launches and no partial buffers: the workspace is the
+ * accumulator alone.  Pairs of one round never share a query chunk, so the
+ * in-place fold is race-free.
+ */
+#define RSA_RING_FUSED_MERGE 1u
+
+/* Workspace bytes for rsa_ring_attn_fwd_ex with these flags. */
+rsa_status rsa_ring_attn_workspace_size_ex(rsa_dtype dt, int B, int H, int64_t T, int d, int N,
+                                           int causal, unsigned flags, size_t *bytes);
+
+/*
+ * rsa_ring_attn_fwd with variant `flags` and optional profiling: when
+ * ev_start, ev_stop and kind are all non-NULL it records events around each
+ * launch as rsa_ring_attn_fwd_timed does (kind 0 block attention, 1 merge);
+ * when all three are NULL nothing is recorded.  *n_launches (if non-NULL)
+ * receives the number of kernel launches.  flags = 0 is rsa_ring_attn_fwd.
+ */
+rsa_status rsa_ring_attn_fwd_ex(const void *q, const void *k, const void *v, rsa_dtype dt,
+                                int B, int H, int64_t T, int d, int N, int causal, unsigned flags,
+                                void *out, float *lse, void *workspace, size_t ws_bytes,
+                                rsa_stream_t stream, rsa_event_t *ev_start, rsa_event_t *ev_stop,
+                                int *kind, int cap, int *n_launches);
+
+/*
  * Host-only view of the ring schedule used by rsa_ring_attn_fwd: the pairs of
  * round r (0-based) as (q_chunk[p], kv_chunk[p]) in host arrays of length
  * `cap`; their count goes to *n_pairs.  No GPU needed.

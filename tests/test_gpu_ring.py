@@ -51,13 +51,14 @@ RING_CASES = [
 ]
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["merge_kernel", "fused_merge"])
 @pytest.mark.parametrize("case", RING_CASES, ids=lambda c: "B{}H{}T{}d{}N{}_{}_{}".format(
     *c[:5], "causal" if c[5] else "full", "bf16" if c[6] == torch.bfloat16 else "f32"))
-def test_ring_matches_oracle(case):
+def test_ring_matches_oracle(case, fused):
     need_cuda()
     B, H, T, d, N, causal, dtype = case
     (q, k, v), (qd, kd, vd) = qkv_cuda(B, H, T, d, dtype, seed=T + N)
-    out, lse = rsa.ring_attn(qd, kd, vd, N, causal)
+    out, lse = rsa.ring_attn(qd, kd, vd, N, causal, fused=fused)
     torch.cuda.synchronize()
     rsa.check_device_error()
     ro, rl = oracle.attention(q, k, v, causal)
@@ -171,3 +172,25 @@ def test_unsupported_and_invalid_calls_raise():
     q = torch.zeros(1, 1, 256, 128, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(rsa.RsaError):
         rsa.ring_attn(q, q, q, 3, True)
+
+
+def test_fused_and_unfused_rings_agree_and_fused_launches_only_block_kernels():
+    need_cuda()
+    B, H, T, d, N = 2, 4, 4096, 128, 8
+    (q, k, v), (qd, kd, vd) = qkv_cuda(B, H, T, d, torch.bfloat16, seed=12)
+    o_a, l_a = rsa.ring_attn(qd, kd, vd, N, True)
+    n = rsa.ring_launch_count(N, True, fused=True)
+    assert n == N
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    out = torch.empty_like(qd)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
+    ws = torch.empty(rsa.workspace_size(torch.bfloat16, B, H, T, d, N, True, fused=True), dtype=torch.uint8,
+                     device="cuda")
+    kinds = rsa.ring_attn_timed(qd, kd, vd, N, True, out, lse, ws, ev0, ev1, fused=True)
+    torch.cuda.synchronize()
+    assert kinds == [0] * N
+    # both orders of folding are the same rounds and the same merge rule
+    assert (out.float() - o_a.float()).abs().max().item() <= 2e-2
+    assert (lse - l_a).abs().max().item() <= 1e-3
+    assert torch.equal(out[:, :, :T // N], o_a[:, :, :T // N])  # chunk 0 is never merged

@@ -14,12 +14,13 @@ from gpu_helpers import assert_close, need_cuda
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["merge_kernel", "fused_merge"])
 @pytest.mark.parametrize("name", ["page1_causal_bf16", "ragged_causal_bf16", "million_causal_bf16"])
-def test_full_size_workload_sampled_rows(name):
+def test_full_size_workload_sampled_rows(name, fused):
     need_cuda()
     w = rsa_inputs.WORKLOADS[name]
     q, k, v = rsa_inputs.make_workload(w, seed=0, device="cuda")
-    out, lse = rsa.ring_attn(q, k, v, w.N, w.causal)
+    out, lse = rsa.ring_attn(q, k, v, w.N, w.causal, fused=fused)
     torch.cuda.synchronize()
     rsa.check_device_error()
     rows = rsa_inputs.sample_rows(w, n=4096, seed=1)
@@ -33,4 +34,4 @@ def test_full_size_workload_sampled_rows(name):
     torch.cuda.empty_cache()
     ro, rl = oracle.attend_rows(q_rows, k_h, v_h, rows, w.causal)
     stats = assert_close(g_out, g_lse, ro, rl, torch.bfloat16, what=name)
-    print(name, stats)
+    print(name, 'fused' if fused else 'merge_kernel', stats)

@@ -73,6 +73,8 @@ def test_workspace_size():
     blk = (N - 1) * B * H * Tc * d * 4 + (N - 1) * B * H * Tc * 4  # fp32 partials
     assert ws == acc + blk
     assert rsa.workspace_size(torch.bfloat16, 1, 1, 256, 128, 1, True) == 0
+    assert rsa.workspace_size(torch.bfloat16, B, H, T, d, N, True, fused=True) == acc
+    assert rsa.ring_launch_count(4, True, fused=True) == 4
     # non-causal rounds have N pairs
     ws2 = rsa.workspace_size(torch.float32, 1, 1, 256, 64, 4, False)
     assert ws2 == 256 * 64 * 4 + 4 * 64 * 64 * 4 + 4 * 64 * 4
