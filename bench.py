@@ -64,6 +64,25 @@ def read_peaks():
         return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+def block_traffic():
+    """Per-launch DRAM traffic of the block kernel from the committed ncu
+    capture, or None if the kernel sources changed since it was taken."""
+    import hashlib
+    path = os.path.join(_ROOT, "profiles", "block_attn_bf16_page1_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        m = hashlib.sha256()
+        for src in rec["sources"]:
+            with open(os.path.join(_ROOT, src), "rb") as f:
+                m.update(f.read())
+        if m.hexdigest()[:16] != rec["source_sha256_16"]:
+            return None
+        return rec["traffic_bytes_per_launch_mean"]
+    except Exception:
+        return None
+
+
 class ClockSampler:
     """nvidia-smi clock and throttle-reason sampling during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -357,7 +376,8 @@ def main():
             "pct_bf16_peak": 100.0 * value / world / peaks["bf16_tflops_sustained"],
             "roofline": {"bound": "tensor", "achieved": blk_tflops, "peak": peaks["bf16_tflops_sustained"],
                          "unit": "TFLOP/s", "frac": blk_tflops / peaks["bf16_tflops_sustained"],
-                         "traffic": None, "kernel": "block_attn_bf16_kernel<128>",
+                         "traffic": block_traffic() if w.name == "page1_causal_bf16" else None,
+                         "kernel": "block_attn_bf16_kernel<128>",
                          "launches_per_step": n_blk, "ms_per_step": blk_ms,
                          "peak_source": peaks["source"] + " bf16_tflops_sustained"},
             "merge": {"bound": "hbm", "achieved": mrg_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
