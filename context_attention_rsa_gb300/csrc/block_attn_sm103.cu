@@ -194,25 +194,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && n > 0) {
             const uint32_t idesc_qk = ptx::idesc_bf16_f32(128, 128, false);
             const uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, true);
+            // Descriptors of the first K step of each operand; a later step only
+            // moves the start address (the low 14 bits, in 16-byte units), which
+            // never carries out of the field inside one tile.
+            const uint64_t dq0 = ptx::smem_desc_sw128(sQ, 16, 1024);
+            const uint64_t dkv0 = ptx::smem_desc_sw128(sKV, 16, 1024);
+            const uint64_t dv0 = ptx::smem_desc_sw128(sKV, C::kBoxBytes, 1024);
             auto issue_qk = [&](int t, int slot) {
-                const uint32_t qa = sQ + t * C::kTileBytes;
-                const uint32_t kb = sKV + slot * C::kTileBytes;
+                const uint64_t qa = dq0 + ((t * C::kTileBytes) >> 4);
+                const uint64_t kb = dkv0 + ((slot * C::kTileBytes) >> 4);
                 const uint32_t dst = tmem + (t ? C::kColS1 : C::kColS0);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-                    ptx::mma_ss(dst, ptx::smem_desc_sw128(qa + off, 16, 1024),
-                                ptx::smem_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
+                    const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+                    ptx::mma_ss(dst, qa + off, kb + off, idesc_qk, kk > 0);
                 }
             };
             auto issue_pv = [&](int t, int slot, bool acc) {
-                const uint32_t vb = sKV + slot * C::kTileBytes;
+                const uint64_t vb = dv0 + ((slot * C::kTileBytes) >> 4);
                 const uint32_t dst = tmem + (t ? C::kColO1 : C::kColO0);
                 const uint32_t pa = tmem + (t ? C::kColS1 : C::kColS0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    ptx::mma_ts(dst, pa + kk * 8, ptx::smem_desc_sw128(vb + kk * 2048, C::kBoxBytes, 1024),
-                                idesc_pv, (acc || kk > 0) ? 1u : 0u);
+                    ptx::mma_ts(dst, pa + kk * 8, vb + ((kk * 2048) >> 4), idesc_pv, (acc || kk > 0) ? 1u : 0u);
             };
             bool ok = ptx::mbar_wait(BAR(C::kQF), 0, lim_ns, abort_flag, p.err, 10);
             int kslot = 0;

@@ -165,6 +165,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
 
 // ---- tcgen05: MMA and commit -----------------------------------------------------
 
+// The MMA wrappers are volatile (they keep their order with the barrier waits
+// and commits around them) but carry no memory clobber: their operands are
+// read through the async proxy and ordered by mbarriers, and leaving ordinary
+// memory alone lets the compiler compute the next descriptors early.
+
 // D[tmem] (+)= A[smem] * B[smem]^T  (one elected thread)
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate)
@@ -173,8 +178,7 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
         "{\n\t.reg .pred P1;\n\t"
         "setp.ne.b32 P1, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, P1;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]  (one elected thread)
@@ -185,8 +189,7 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "{\n\t.reg .pred P1;\n\t"
         "setp.ne.b32 P1, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, P1;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // Arrive once on `bar` when every tcgen05 async operation this thread issued
