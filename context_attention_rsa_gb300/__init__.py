@@ -281,31 +281,74 @@ def ring_launch_count(N: int, causal: bool, fused: bool = False) -> int:
 
 
 def ring_attn_from_host(q_host, k_host, v_host, N: int, causal: bool, device=None, stream=None,
-                        buffers=None):
-    """End-to-end call from host memory: copy Q, K, V (ideally pinned) to the
-    device, run the ring, and copy out and lse back into host tensors.
-    ``buffers`` may hold reusable device/host tensors (q, k, v, out, lse, ws,
-    out_host, lse_host) to keep allocation out of a timed loop."""
+                        buffers=None, groups: int = 8):
+    """End-to-end call from host memory: Q, K, V (host tensors, ideally pinned)
+    in, out and lse (pinned host tensors) back.
+
+    Heads are independent problems, so the B*H heads are cut into ``groups``
+    contiguous slabs that stream through three CUDA streams: the copy of slab
+    g+1 to the device, the ring on slab g (C ABI, on ``stream`` or the current
+    stream) and the copy of slab g-1 back to the host all overlap.  Device
+    slabs are double-buffered.  The returned host tensors are complete once
+    ``stream`` has passed the call (it waits for the last copy back).
+    ``buffers`` (a dict, filled on first use) keeps the device slabs, the
+    workspace, the pinned outputs and the copy streams for reuse."""
     dev = torch.device(device) if device is not None else torch.device("cuda")
     b = buffers if buffers is not None else {}
     B, H, T, d = q_host.shape
-    if "q" not in b:
-        b["q"] = torch.empty(q_host.shape, dtype=q_host.dtype, device=dev)
-        b["k"] = torch.empty(q_host.shape, dtype=q_host.dtype, device=dev)
-        b["v"] = torch.empty(q_host.shape, dtype=q_host.dtype, device=dev)
-        b["out"] = torch.empty(q_host.shape, dtype=q_host.dtype, device=dev)
-        b["lse"] = torch.empty((B, H, T), dtype=torch.float32, device=dev)
-        b["ws"] = torch.empty(max(workspace_size(q_host.dtype, B, H, T, d, N, causal), 1),
-                              dtype=torch.uint8, device=dev)
+    BH = B * H
+    G = max(1, min(int(groups), BH))
+    hg = (BH + G - 1) // G  # heads per slab
+    G = (BH + hg - 1) // hg
+    main = torch.cuda.current_stream(dev) if stream is None else stream
+    key = (tuple(q_host.shape), q_host.dtype, N, bool(causal), hg, str(dev))
+    if b.get("key") != key:
+        b.clear()
+        b["key"] = key
+        mk = lambda *shape, dt=q_host.dtype: torch.empty(shape, dtype=dt, device=dev)
+        b["in"] = [[mk(hg, T, d) for _ in range(3)] for _ in range(2)]
+        b["out"] = [mk(hg, T, d) for _ in range(2)]
+        b["lse"] = [mk(hg, T, dt=torch.float32) for _ in range(2)]
+        b["ws"] = mk(max(workspace_size(q_host.dtype, 1, hg, T, d, N, causal), 1), dt=torch.uint8)
         b["out_host"] = torch.empty(q_host.shape, dtype=q_host.dtype, pin_memory=True)
         b["lse_host"] = torch.empty((B, H, T), dtype=torch.float32, pin_memory=True)
-    b["q"].copy_(q_host, non_blocking=True)
-    b["k"].copy_(k_host, non_blocking=True)
-    b["v"].copy_(v_host, non_blocking=True)
-    ring_attn(b["q"], b["k"], b["v"], N, causal, out=b["out"], lse=b["lse"], workspace=b["ws"],
-              stream=stream)
-    b["out_host"].copy_(b["out"], non_blocking=True)
-    b["lse_host"].copy_(b["lse"], non_blocking=True)
+        b["s_in"] = torch.cuda.Stream(dev)
+        b["s_out"] = torch.cuda.Stream(dev)
+    s_in, s_out = b["s_in"], b["s_out"]
+    src = [t.reshape(BH, T, d) for t in (q_host, k_host, v_host)]
+    oh = b["out_host"].view(BH, T, d)
+    lh = b["lse_host"].view(BH, T)
+    s_in.wait_stream(main)
+    s_out.wait_stream(main)
+    ev_comp, ev_out = [], []
+    for g in range(G):
+        h0, h1 = g * hg, min(BH, (g + 1) * hg)
+        n = h1 - h0
+        slot = g % 2
+        with torch.cuda.stream(s_in):
+            if g >= 2:
+                s_in.wait_event(ev_comp[g - 2])  # ring on slab g-2 has read this slot
+            for t_dev, t_host in zip(b["in"][slot], src):
+                t_dev[:n].copy_(t_host[h0:h1], non_blocking=True)
+            ev_in = torch.cuda.Event()
+            ev_in.record(s_in)
+        main.wait_event(ev_in)
+        if g >= 2:
+            main.wait_event(ev_out[g - 2])  # slab g-2 has been copied out of this slot
+        qd, kd, vd = (t[:n].view(1, n, T, d) for t in b["in"][slot])
+        ring_attn(qd, kd, vd, N, causal, out=b["out"][slot][:n].view(1, n, T, d),
+                  lse=b["lse"][slot][:n].view(1, n, T), workspace=b["ws"], stream=main)
+        ev = torch.cuda.Event()
+        ev.record(main)
+        ev_comp.append(ev)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev)
+            oh[h0:h1].copy_(b["out"][slot][:n], non_blocking=True)
+            lh[h0:h1].copy_(b["lse"][slot][:n], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(s_out)
+            ev_out.append(ev)
+    main.wait_event(ev_out[-1])
     return b["out_host"], b["lse_host"], b
 
 

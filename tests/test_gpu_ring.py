@@ -194,3 +194,18 @@ def test_fused_and_unfused_rings_agree_and_fused_launches_only_block_kernels():
     assert (out.float() - o_a.float()).abs().max().item() <= 2e-2
     assert (lse - l_a).abs().max().item() <= 1e-3
     assert torch.equal(out[:, :, :T // N], o_a[:, :, :T // N])  # chunk 0 is never merged
+
+
+@pytest.mark.parametrize("groups", [1, 3, 8])
+def test_ring_from_host_matches_device_ring(groups):
+    # The streamed host-to-host path (head slabs through three streams) gives
+    # exactly the device ring's result: every head is its own problem.
+    need_cuda()
+    B, H, T, d, N = 2, 5, 1024, 128, 4
+    q, k, v = (t.pin_memory() for t in qkv_cuda(B, H, T, d, torch.bfloat16, seed=13)[0])
+    ref_o, ref_l = rsa.ring_attn(q.cuda(), k.cuda(), v.cuda(), N, True)
+    bufs = {}
+    for _ in range(2):  # second call reuses the buffers
+        oh, lh, bufs = rsa.ring_attn_from_host(q, k, v, N, True, buffers=bufs, groups=groups)
+        torch.cuda.synchronize()
+        assert torch.equal(oh, ref_o.cpu()) and torch.equal(lh, ref_l.cpu())
