@@ -24,7 +24,7 @@ from . import _build
 
 __all__ = [
     "RsaError", "load", "library_path", "block_attn_fwd", "merge", "merge_finalize",
-    "ring_attn", "ring_attn_noalloc", "ring_attn_timed", "ring_attn_from_host", "workspace_size", "ring_schedule",
+    "ring_attn", "ring_attn_noalloc", "ring_attn_timed", "decode_attn", "decode_workspace_size", "ring_attn_from_host", "workspace_size", "ring_schedule",
     "set_wait_limit_ns", "check_device_error", "selftest_wait_timeout", "version",
     "RSA_F32", "RSA_BF16",
 ]
@@ -71,6 +71,9 @@ _SIGS = {
                              ctypes.c_uint, _c_void_p, _c_void_p, _c_void_p, ctypes.c_size_t, _c_void_p,
                              ctypes.POINTER(_c_void_p), ctypes.POINTER(_c_void_p), ctypes.POINTER(_i32),
                              _i32, ctypes.POINTER(_i32)],
+    "rsa_decode_workspace_size": [_i32, _i32, _i32, _i64, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)],
+    "rsa_decode_attn_fwd": [_c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _i64, _i32, _i32, _i32, _i32,
+                            _c_void_p, _c_void_p, _c_void_p, ctypes.c_size_t, _c_void_p],
     "rsa_ring_schedule": [_i32, _i32, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _i32,
                           ctypes.POINTER(_i32)],
     "rsa_set_wait_limit_ns": [ctypes.c_uint64],
@@ -350,6 +353,39 @@ def ring_attn_from_host(q_host, k_host, v_host, N: int, causal: bool, device=Non
             ev_out.append(ev)
     main.wait_event(ev_out[-1])
     return b["out_host"], b["lse_host"], b
+
+
+def decode_workspace_size(dtype: torch.dtype, B: int, H: int, T: int, d: int, q_len: int, N: int) -> int:
+    n = ctypes.c_size_t(0)
+    dt = RSA_F32 if dtype == torch.float32 else RSA_BF16
+    _call("rsa_decode_workspace_size", dt, B, H, T, d, q_len, N, ctypes.byref(n))
+    return int(n.value)
+
+
+def decode_attn(q, k, v, N: int, causal: bool, out=None, lse=None, workspace=None,
+                stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Decode against a KV cache cut into N shards: q [B, H, q_len, d] holds the
+    q_len newest tokens (positions T-q_len .. T-1), k and v [B, H, T, d] the
+    cache.  Returns (out [B, H, q_len, d], lse [B, H, q_len] fp32)."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-d CUDA tensor")
+    if k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3] or not (
+            q.dtype == k.dtype == v.dtype):
+        raise ValueError("q [B, H, q_len, d] and k, v [B, H, T, d] must agree")
+    B, H, q_len, d = q.shape
+    T = k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, q_len), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(max(decode_workspace_size(q.dtype, B, H, T, d, q_len, N), 1), dtype=torch.uint8,
+                                device=q.device)
+    _call("rsa_decode_attn_fwd", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, q_len, N,
+          int(bool(causal)), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+          workspace.numel() * workspace.element_size(), _stream(stream))
+    return out, lse
 
 
 def ring_schedule(N: int, causal: bool, rnd: int) -> List[Tuple[int, int]]:

@@ -50,21 +50,24 @@ __global__ void __launch_bounds__(kWarps * 32)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t r = (int64_t)blockIdx.x * kWarps + warp;
     const int bh = blockIdx.y;
-    const PairDesc &pr = p.pairs[blockIdx.z];
+    const int sp = blockIdx.z / p.npairs;  // key split (decode), 0 otherwise
+    const PairDesc &pr = p.pairs[blockIdx.z - sp * p.npairs];
     if (r >= p.q_len)
         return;  // whole warp leaves together
     const int64_t qpos = pr.q_off + r;
     const int64_t head = (int64_t)bh * p.T;
+    const int64_t kv_off = pr.kv_off + (int64_t)sp * p.kv_split;
+    const int64_t kv_len = p.kv_split > 0 ? min(p.kv_split, p.kv_len - (int64_t)sp * p.kv_split) : p.kv_len;
     const float scale = 1.0f / sqrtf((float)D);
-    const float *qrow = q + (head + qpos) * D;
+    const float *qrow = q + ((int64_t)bh * p.q_T + pr.q_row0 + r) * D;
 #pragma unroll
     for (int i = 0; i < PER; ++i)
         qs[warp][lane + 32 * i] = qrow[lane + 32 * i];
     __syncwarp();
 
-    int64_t kv_end = p.kv_len;
+    int64_t kv_end = kv_len;
     if (p.causal)
-        kv_end = min(kv_end, qpos - pr.kv_off + 1);
+        kv_end = min(kv_end, qpos - kv_off + 1);
     float m = -INFINITY, l = 0.f;
     float o[PER];
 #pragma unroll
@@ -75,7 +78,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         const int64_t j = j0 + lane;
         float s = -INFINITY;
         if (j < kv_end) {
-            const float4 *kr = reinterpret_cast<const float4 *>(k + (head + pr.kv_off + j) * D);
+            const float4 *kr = reinterpret_cast<const float4 *>(k + (head + kv_off + j) * D);
             const float4 *qv = reinterpret_cast<const float4 *>(qs[warp]);
             float dot = 0.f;
 #pragma unroll 8
@@ -96,7 +99,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         for (int i = 0; i < PER; ++i)
             o[i] *= alpha;
         const int nk = (int)min((int64_t)32, kv_end - j0);
-        const float *vb = v + (head + pr.kv_off + j0) * D;
+        const float *vb = v + (head + kv_off + j0) * D;
         for (int kk = 0; kk < nk; ++kk) {
             const float pk = __shfl_sync(0xffffffffu, pj, kk);
 #pragma unroll
@@ -106,7 +109,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         m = m_new;
     }
 
-    const int64_t orow = (int64_t)bh * pr.out_T + pr.out_t0 + r;
+    const int64_t orow = (int64_t)bh * pr.out_T + pr.out_t0 + r + (int64_t)sp * pr.split_stride;
     const bool empty = !(l > 0.f);
     const float lse_b = empty ? -INFINITY : m + logf(l);
     float wa = 0.f, wb = empty ? 0.f : 1.f / l, lse_out = lse_b;
@@ -143,9 +146,10 @@ cudaError_t launch_block_attn_f32(const float *q, const float *k, const float *v
     const int64_t BH = (int64_t)p.B * p.H;
     if (bx <= 0 || BH <= 0 || p.npairs <= 0)
         return cudaSuccess;
-    if (bx > 0x7fffffffLL || BH > 65535)
+    const int64_t bz = (int64_t)p.npairs * p.n_split;
+    if (bx > 0x7fffffffLL || BH > 65535 || bz > 65535)
         return cudaErrorInvalidConfiguration;
-    dim3 grid((unsigned)bx, (unsigned)BH, (unsigned)p.npairs);
+    dim3 grid((unsigned)bx, (unsigned)BH, (unsigned)bz);
     if (p.d == 64)
         block_attn_f32_kernel<64><<<grid, kWarps * 32, 0, s>>>(q, k, v, p);
     else if (p.d == 128)

@@ -114,17 +114,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // All row groups of one (pair, head) are consecutive blocks, so the CTAs
     // running at the same time stream the same K/V chunk and share it in L2.
     // Inside a (pair, head) the heaviest causal groups come first.
+    // A pair's key range may be cut into n_split splits (decode): each split
+    // is its own work unit and writes its own partial rows.
     const int64_t L = blockIdx.x;
     const int64_t unit = L / p.n_qgroups;
     const int qg = p.n_qgroups - 1 - (int)(L - unit * p.n_qgroups);
-    const int pi = (int)(unit % p.npairs);
-    const int bh = (int)(unit / p.npairs);
+    const int sp = (int)(unit % p.n_split);
+    const int64_t unit2 = unit / p.n_split;
+    const int pi = (int)(unit2 % p.npairs);
+    const int bh = (int)(unit2 / p.npairs);
     const PairDesc &pr = p.pairs[pi];
+    const int64_t kv_off = pr.kv_off + (int64_t)sp * p.kv_split;
+    const int64_t kv_len = p.kv_split > 0 ? min(p.kv_split, p.kv_len - (int64_t)sp * p.kv_split) : p.kv_len;
     const int64_t q0 = (int64_t)qg * kBf16RowsPerCta;
     const int64_t rows_valid = min((int64_t)kBf16RowsPerCta, p.q_len - q0);
-    int64_t kv_end = p.kv_len;
+    int64_t kv_end = kv_len;
     if (p.causal)
-        kv_end = min(kv_end, pr.q_off + q0 + rows_valid - pr.kv_off);
+        kv_end = min(kv_end, pr.q_off + q0 + rows_valid - kv_off);
     const int n = kv_end > 0 ? (int)((kv_end + 127) / 128) : 0;
 
     if (threadIdx.x == 0) {
@@ -167,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < 2; ++t)
                 for (int b = 0; b < C::kBoxes; ++b)
                     ptx::tma_load_3d(sQ + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, BAR(C::kQF),
-                                     b * 64, (int)(pr.q_off + q0 + t * 128), bh);
+                                     b * 64, (int)(pr.q_row0 + q0 + t * 128), bh);
             for (int ld = 0; ld < 2 * n; ++ld) {
                 const int slot = ld % C::kStages;
                 const int use = ld / C::kStages;
@@ -175,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     !ptx::mbar_wait(BAR(C::kKVE + slot), (use - 1) & 1, lim_ns, abort_flag, p.err, 1))
                     break;
                 const CUtensorMap *m = (ld & 1) ? &tm_v : &tm_k;
-                const int row = (int)(pr.kv_off + (int64_t)(ld >> 1) * 128);
+                const int row = (int)(kv_off + (int64_t)(ld >> 1) * 128);
                 ptx::mbar_arrive_expect_tx(BAR(C::kKVF + slot), C::kTileBytes);
                 for (int b = 0; b < C::kBoxes; ++b)
                     ptx::tma_load_3d(sKV + slot * C::kTileBytes + b * C::kBoxBytes, m,
@@ -286,9 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lane_addr + (t ? C::kColS1 : C::kColS0);
         const uint32_t tO = tmem + lane_addr + (t ? C::kColO1 : C::kColO0);
         const float sl2 = 1.4426950408889634f / sqrtf((float)D);  // log2(e) / sqrt(d)
-        int64_t allowed = p.kv_len;  // keys [0, allowed) of the pair are visible to this row
+        int64_t allowed = kv_len;  // keys [0, allowed) of this split are visible to this row
         if (p.causal)
-            allowed = min(allowed, qpos - pr.kv_off + 1);
+            allowed = min(allowed, qpos - kv_off + 1);
         float m_used = -INFINITY;  // kept maximum, log2 units
         float l = 0.f;
         bool ok = true;
@@ -388,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // M = max(a, b), L = M + ln(e^{a-M} + e^{b-M}), o = acc e^{a-L} + o_b e^{b-L}.
             const bool empty = !(l > 0.f);
             const bool valid = rg < p.q_len;
-            const int64_t orow = (int64_t)bh * pr.out_T + pr.out_t0 + rg;
+            const int64_t orow = (int64_t)bh * pr.out_T + pr.out_t0 + rg + (int64_t)sp * pr.split_stride;
             const float lse_b = empty ? -INFINITY : (m_used + ptx::lg2(l)) * 0.69314718055994531f;
             float wa = 0.f;                           // weight of the accumulator row
             float wb = empty ? 0.f : 1.f / l;         // weight of the unnormalised O row
@@ -508,9 +514,9 @@ cudaError_t launch_d(const void *q, const void *k, const void *v, const BlockPar
 {
     const int64_t BH = (int64_t)p.B * p.H;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, q, BH, p.T, D) || !make_map(&mk, k, BH, p.T, D) || !make_map(&mv, v, BH, p.T, D))
+    if (!make_map(&mq, q, BH, p.q_T, D) || !make_map(&mk, k, BH, p.T, D) || !make_map(&mv, v, BH, p.T, D))
         return cudaErrorInvalidValue;
-    const int64_t grid = (int64_t)p.n_qgroups * p.npairs * BH;
+    const int64_t grid = (int64_t)p.n_qgroups * p.npairs * BH * p.n_split;
     if (grid <= 0)
         return cudaSuccess;
     if (grid > 0x7fffffffLL)

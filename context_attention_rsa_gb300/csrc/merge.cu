@@ -135,7 +135,81 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// Fold S partial results of the same rows (split-KV decode): one warp per row.
+// M = max_s lse_s, L = M + ln sum_s e^{lse_s - M}, o = sum_s o_s e^{lse_s - L};
+// rows whose partials are all empty stay (0, -inf).
+template <int PER>
+__global__ void __launch_bounds__(256)
+    merge_splits_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part, int S, int64_t rows,
+                        void *out, int out_f32, float *lse)
+{
+    constexpr int D = PER * 32;
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows)
+        return;
+    float M = -INFINITY;
+    for (int s = lane; s < S; s += 32)
+        M = fmaxf(M, lse_part[(int64_t)s * rows + row]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float acc[PER];
+#pragma unroll
+    for (int c = 0; c < PER; ++c)
+        acc[c] = 0.f;
+    float L = -INFINITY;
+    if (M > -INFINITY) {
+        float sum = 0.f;
+        for (int s = lane; s < S; s += 32)
+            sum += expf(lse_part[(int64_t)s * rows + row] - M);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        L = M + logf(sum);
+        for (int s = 0; s < S; ++s) {
+            const float w = expf(lse_part[(int64_t)s * rows + row] - L);
+            if (w == 0.f)
+                continue;
+            const float *src = o_part + ((int64_t)s * rows + row) * D + lane * PER;
+#pragma unroll
+            for (int c = 0; c < PER; ++c)
+                acc[c] = fmaf(w, src[c], acc[c]);
+        }
+    }
+    if (out_f32) {
+        float *dst = static_cast<float *>(out) + row * D + lane * PER;
+#pragma unroll
+        for (int c = 0; c < PER; ++c)
+            dst[c] = acc[c];
+    } else {
+        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(out) + row * D + lane * PER;
+#pragma unroll
+        for (int c = 0; c < PER; c += 2)
+            *reinterpret_cast<uint32_t *>(dst + c) = pack2(acc[c], acc[c + 1]);
+    }
+    if (lane == 0)
+        lse[row] = L;
+}
+
 }  // namespace
+
+cudaError_t launch_merge_splits(const float *o_part, const float *lse_part, int S, int64_t rows, int d, void *out,
+                                int out_f32, float *lse, cudaStream_t s)
+{
+    if (rows <= 0 || S <= 0)
+        return cudaSuccess;
+    const int64_t blocks = (rows + 7) / 8;
+    if (blocks > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    if (d == 128)
+        merge_splits_kernel<4><<<(unsigned)blocks, 256, 0, s>>>(o_part, lse_part, S, rows, out, out_f32, lse);
+    else if (d == 64)
+        merge_splits_kernel<2><<<(unsigned)blocks, 256, 0, s>>>(o_part, lse_part, S, rows, out, out_f32, lse);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
 
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t s)
 {

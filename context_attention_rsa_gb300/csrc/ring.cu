@@ -246,6 +246,8 @@ BlockParams base_params(rsa_dtype dt, int B, int H, int64_t T, int d, int causal
     p.causal = causal ? 1 : 0;
     p.q_len = q_len;
     p.kv_len = kv_len;
+    p.q_T = T;
+    p.n_split = 1;
     p.n_qgroups = (int)((q_len + kBf16RowsPerCta - 1) / kBf16RowsPerCta);
     p.wait_limit_ns = g_wait_limit_ns.load();
     p.err = err;
@@ -298,6 +300,7 @@ rsa_status ring_run(const void *q, const void *k, const void *v, rsa_dtype dt, i
             PairDesc &pd = p.pairs[p.npairs++];
             const bool once = visits(N, causal, i) == 1;
             pd.q_off = i * Tc;
+            pd.q_row0 = pd.q_off;
             pd.kv_off = i * Tc;
             pd.out = once ? out : static_cast<void *>(o_acc);
             pd.lse = lse;
@@ -320,6 +323,7 @@ rsa_status ring_run(const void *q, const void *k, const void *v, rsa_dtype dt, i
                     const bool last = r == visits(N, causal, i) - 1;
                     PairDesc &pd = p.pairs[p.npairs++];
                     pd.q_off = i * Tc;
+                    pd.q_row0 = pd.q_off;
                     pd.kv_off = j * Tc;
                     pd.out = last ? out : static_cast<void *>(o_acc);
                     pd.lse = lse;
@@ -355,6 +359,7 @@ rsa_status ring_run(const void *q, const void *k, const void *v, rsa_dtype dt, i
                 float *lb = lblk + (size_t)slot * (size_t)BH * Tc;
                 PairDesc &pd = p.pairs[p.npairs++];
                 pd.q_off = i * Tc;
+                pd.q_row0 = pd.q_off;
                 pd.kv_off = j * Tc;
                 pd.out = ob;
                 pd.lse = lb;
@@ -374,9 +379,113 @@ rsa_status ring_run(const void *q, const void *k, const void *v, rsa_dtype dt, i
     return RSA_OK;
 }
 
+// Split-KV decode layout.  The cache of T keys is cut into N shards of T/N
+// keys; each shard is cut further into splits of kv_split keys (a multiple of
+// 128, at least 1024 unless a shard is shorter) so that about 2048 CTAs run.
+// Every split writes an fp32 partial (o, lse) for every query row.
+struct DecodeLayout {
+    int64_t kv_split;
+    int sps;  // splits per shard
+    int S;    // splits in total
+    size_t part_o, part_lse, total;
+};
+
+DecodeLayout decode_layout(int B, int H, int64_t T, int d, int64_t q_len, int N)
+{
+    DecodeLayout L{};
+    const int64_t Tc = T / N;
+    const int64_t BH = (int64_t)B * H;
+    const int64_t groups = (q_len + kBf16RowsPerCta - 1) / kBf16RowsPerCta;
+    int64_t want = (2048 + BH * N * groups - 1) / (BH * N * groups);
+    if (want < 1)
+        want = 1;
+    int64_t ks = ((Tc + want - 1) / want + 127) / 128 * 128;
+    if (ks < 1024)
+        ks = 1024;
+    if (ks > Tc)
+        ks = Tc;
+    L.kv_split = ks;
+    L.sps = (int)((Tc + ks - 1) / ks);
+    L.S = N * L.sps;
+    L.part_o = align256((size_t)L.S * BH * q_len * d * 4);
+    L.part_lse = align256((size_t)L.S * BH * q_len * 4);
+    L.total = L.part_o + L.part_lse;
+    return L;
+}
+
+rsa_status check_decode(rsa_dtype dt, int B, int H, int64_t T, int d, int q_len, int N)
+{
+    RSA_TRY(check_shape(dt, B, H, T, d));
+    if (q_len < 1 || q_len > T)
+        return fail(RSA_ERR_INVALID_ARG, "q_len=%d must be in [1, T=%lld]", q_len, (long long)T);
+    if (N < 1 || N > T || T % N != 0)
+        return fail(RSA_ERR_INVALID_ARG, "N=%d must be >= 1 and divide T=%lld", N, (long long)T);
+    if (N > 1024)
+        return fail(RSA_ERR_UNSUPPORTED, "N=%d exceeds 1024 shards", N);
+    return RSA_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+rsa_status rsa_decode_workspace_size(rsa_dtype dt, int B, int H, int64_t T, int d, int q_len, int N, size_t *bytes)
+{
+    if (!bytes)
+        return fail(RSA_ERR_INVALID_ARG, "bytes is NULL");
+    RSA_TRY(check_decode(dt, B, H, T, d, q_len, N));
+    *bytes = decode_layout(B, H, T, d, q_len, N).total;
+    return RSA_OK;
+}
+
+rsa_status rsa_decode_attn_fwd(const void *q, const void *k, const void *v, rsa_dtype dt, int B, int H, int64_t T,
+                               int d, int q_len, int N, int causal, void *out, float *lse, void *workspace,
+                               size_t ws_bytes, rsa_stream_t stream)
+{
+    RSA_TRY(check_decode(dt, B, H, T, d, q_len, N));
+    RSA_TRY(check_ptr(q, "q"));
+    RSA_TRY(check_ptr(k, "k"));
+    RSA_TRY(check_ptr(v, "v"));
+    RSA_TRY(check_ptr(out, "out"));
+    RSA_TRY(check_ptr(lse, "lse"));
+    const DecodeLayout lay = decode_layout(B, H, T, d, q_len, N);
+    RSA_TRY(check_ptr(workspace, "workspace"));
+    if (ws_bytes < lay.total)
+        return fail(RSA_ERR_INVALID_ARG, "workspace holds %zu bytes, %zu needed", ws_bytes, lay.total);
+    RSA_TRY(check_device_for(dt));
+    unsigned int *err = nullptr;
+    RSA_TRY(device_error_word(&err));
+    const int64_t Tc = T / N;
+    const int64_t BH = (int64_t)B * H;
+    float *part_o = static_cast<float *>(workspace);
+    float *part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + lay.part_o);
+    // Shards are the pairs of the block kernel: query rows T-q_len..T-1 (the
+    // newest tokens) against keys [i*Tc, (i+1)*Tc), cut into splits.
+    for (int g0 = 0; g0 < N; g0 += kMaxPairsPerLaunch) {
+        BlockParams p = base_params(dt, B, H, T, d, causal, q_len, Tc, err);
+        p.q_T = q_len;
+        p.kv_split = lay.kv_split;
+        p.n_split = lay.sps;
+        for (int i = g0; i < N && p.npairs < kMaxPairsPerLaunch; ++i) {
+            PairDesc &pd = p.pairs[p.npairs++];
+            pd.q_off = T - q_len;
+            pd.q_row0 = 0;
+            pd.kv_off = i * Tc;
+            pd.out = part_o + (size_t)i * lay.sps * BH * q_len * d;
+            pd.lse = part_lse + (size_t)i * lay.sps * BH * q_len;
+            pd.out_T = q_len;
+            pd.out_t0 = 0;
+            pd.out_f32 = 1;
+            pd.mode = kStore;
+            pd.split_stride = BH * q_len;
+        }
+        RSA_TRY(launch_block(q, k, v, dt, p, stream, nullptr));
+    }
+    cudaError_t e = launch_merge_splits(part_o, part_lse, lay.S, BH * q_len, d, out, dt == RSA_F32, lse, stream);
+    if (e != cudaSuccess)
+        return fail(RSA_ERR_CUDA, "merge of decode splits: %s", cudaGetErrorString(e));
+    return RSA_OK;
+}
 
 rsa_status rsa_block_attn_fwd(const void *q, const void *k, const void *v, rsa_dtype dt, int B, int H, int64_t T,
                               int d, int64_t q_off, int64_t q_len, int64_t kv_off, int64_t kv_len, int causal,
@@ -397,6 +506,7 @@ rsa_status rsa_block_attn_fwd(const void *q, const void *k, const void *v, rsa_d
     BlockParams p = base_params(dt, B, H, T, d, causal, q_len, kv_len, err);
     PairDesc &pd = p.pairs[p.npairs++];
     pd.q_off = q_off;
+    pd.q_row0 = pd.q_off;
     pd.kv_off = kv_off;
     pd.out = o_blk;
     pd.lse = lse_blk;

@@ -30,6 +30,7 @@ enum EpilogueMode : int {
 // at the same index of `acc` (and the running lse from `lse`).
 struct PairDesc {
     int64_t q_off;   // global position of the first query row
+    int64_t q_row0;  // row of the first query inside each head of the Q tensor
     int64_t kv_off;  // global position of the first key
     void *out;       // bf16 or fp32 (out_f32)
     float *lse;
@@ -38,14 +39,18 @@ struct PairDesc {
     int out_f32;     // 1: fp32 output, 0: bf16 output
     int mode;        // EpilogueMode
     const float *acc;  // fp32 accumulator (kMergeAcc: same as out; kMergeFinal: read only)
+    int64_t split_stride;  // out/lse rows between consecutive key splits of this pair
 };
 
 struct BlockParams {
     int B, H;
-    int64_t T;
+    int64_t T;              // rows per head of K and V
+    int64_t q_T;            // rows per head of the Q tensor (T, or the decode rows)
     int d;
     int causal;
     int64_t q_len, kv_len;  // rows per pair, keys per pair
+    int64_t kv_split;       // keys per split of a pair's key range (0: one split)
+    int n_split;            // splits per pair; split s covers keys [s*kv_split, (s+1)*kv_split)
     int npairs;
     int n_qgroups;          // query-row groups per pair (rows per CTA granularity)
     uint64_t wait_limit_ns;
@@ -82,6 +87,9 @@ cudaError_t launch_block_attn_bf16(const void *q, const void *k, const void *v,
 cudaError_t launch_block_attn_f32(const float *q, const float *k, const float *v,
                                   const BlockParams &p, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t s);
+// Fold S partials [S][rows][d] (fp32 o, fp32 lse) into out [rows][d] and lse [rows].
+cudaError_t launch_merge_splits(const float *o_part, const float *lse_part, int S, int64_t rows, int d,
+                                void *out, int out_f32, float *lse, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint64_t limit_ns, unsigned int *err, cudaStream_t s);
 
 // Rows of one CTA of the tensor-core kernel (two 128-row tiles).

@@ -192,6 +192,29 @@ rsa_status rsa_ring_attn_fwd_ex(const void *q, const void *k, const void *v, rsa
                                 int *kind, int cap, int *n_launches);
 
 /*
+ * Decode against a distributed KV cache ([P1] "Training and inference stress
+ * this dimension differently": the history of keys and values is split
+ * across devices, a new query is evaluated against every block and the
+ * partial results are combined).  The cache k, v [B, H, T, d] is cut into N
+ * contiguous shards of T/N keys (here all on this GPU); each shard is cut
+ * further into splits for parallelism.  Every split yields an fp32 partial
+ * (o, lse) for each query row, and the partials are folded with the rule of
+ * rsa_merge.
+ *   q    [B, H, q_len, d]: the q_len newest tokens, at global positions
+ *        T - q_len .. T - 1 (their keys and values are already in the cache)
+ *   out  [B, H, q_len, d] (dtype dt), lse [B, H, q_len] fp32
+ * causal: row r sees keys 0 .. T - q_len + r; otherwise every key.
+ * Requires 1 <= q_len <= T and N dividing T.  `workspace` must hold
+ * rsa_decode_workspace_size() bytes.
+ */
+rsa_status rsa_decode_workspace_size(rsa_dtype dt, int B, int H, int64_t T, int d, int q_len, int N,
+                                     size_t *bytes);
+rsa_status rsa_decode_attn_fwd(const void *q, const void *k, const void *v, rsa_dtype dt,
+                               int B, int H, int64_t T, int d, int q_len, int N, int causal,
+                               void *out, float *lse, void *workspace, size_t ws_bytes,
+                               rsa_stream_t stream);
+
+/*
  * Host-only view of the ring schedule used by rsa_ring_attn_fwd: the pairs of
  * round r (0-based) as (q_chunk[p], kv_chunk[p]) in host arrays of length
  * `cap`; their count goes to *n_pairs.  No GPU needed.

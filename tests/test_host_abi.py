@@ -133,3 +133,23 @@ def test_wait_limit_bounds():
     lib = rsa.load()
     assert lib.rsa_set_wait_limit_ns(10) == 1
     assert lib.rsa_set_wait_limit_ns(2_000_000_000) == 0
+
+
+def test_decode_workspace_and_validation():
+    import torch
+    # 4 x 8 heads, million-token cache in 16 shards: 32 x 16 = 512 (head, shard)
+    # units, so each shard is cut into 4 splits of 16384 keys (about 2048 CTAs)
+    B, H, T, d, N, ql = 4, 8, 1 << 20, 128, 16, 1
+    ws = rsa.decode_workspace_size(torch.bfloat16, B, H, T, d, ql, N)
+    S = N * 4
+    assert ws == (S * B * H * ql * d * 4 + 255) // 256 * 256 + (S * B * H * ql * 4 + 255) // 256 * 256
+    lib = rsa.load()
+    args = [FAKE, FAKE, FAKE, 1, 1, 1, 256, 128, 1, 4, 1, FAKE, FAKE, FAKE, 1 << 40, None]
+    bad = list(args); bad[8] = 0          # q_len 0
+    assert lib.rsa_decode_attn_fwd(*bad) == 1
+    bad = list(args); bad[8] = 300        # q_len > T
+    assert lib.rsa_decode_attn_fwd(*bad) == 1
+    bad = list(args); bad[9] = 3          # N does not divide T
+    assert lib.rsa_decode_attn_fwd(*bad) == 1
+    bad = list(args); bad[14] = 16        # workspace too small
+    assert lib.rsa_decode_attn_fwd(*bad) == 1
