@@ -211,6 +211,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fused", action="store_true", help="skip timing the fused-merge ring variant")
+    ap.add_argument("--no-decode", action="store_true", help="skip timing decode on the million-token cache")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--shape", default=None,
                     help="B,H,T,d,N,causal: a bf16 normal-recipe workload instead of --workload (profiling)")
@@ -322,6 +323,42 @@ def main():
               "workspace_bytes": int(ws_f.numel())}
         del ws_f
 
+    # ---- decode against a sharded million-token KV cache (HBM-bound) ---------
+    dec = None
+    if not args.no_decode and world == 1:
+        del ws
+        torch.cuda.empty_cache()
+        wd = rsa_inputs.WORKLOADS["decode_million_bf16"]
+        qd_full, kd, vd = rsa_inputs.make_workload(wd, seed=1, device=dev)
+        qd = qd_full[:, :, wd.T - wd.q_len:].contiguous()
+        del qd_full
+        od = torch.empty_like(qd)
+        ld = torch.empty((wd.B, wd.H, wd.q_len), dtype=torch.float32, device=dev)
+        wsd = torch.empty(rsa.decode_workspace_size(qd.dtype, wd.B, wd.H, wd.T, wd.d, wd.q_len, wd.N),
+                          dtype=torch.uint8, device=dev)
+        for _ in range(max(args.warmup, 0)):
+            rsa.decode_attn(qd, kd, vd, wd.N, wd.causal, out=od, lse=ld, workspace=wsd)
+        torch.cuda.synchronize()
+        d0 = torch.cuda.Event(enable_timing=True)
+        d1 = torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for _ in range(args.steps):
+            rsa.decode_attn(qd, kd, vd, wd.N, wd.causal, out=od, lse=ld, workspace=wsd)
+        d1.record(stream)
+        torch.cuda.synchronize()
+        rsa.check_device_error()
+        d_ms = d0.elapsed_time(d1) / args.steps
+        # algorithmic bytes: the whole K and V cache once, the queries and the outputs
+        dbytes = 2 * kd.numel() * kd.element_size() + 2 * qd.numel() * qd.element_size() + ld.numel() * 4
+        dec = {"workload": wd.name, "B": wd.B, "H": wd.H, "T": wd.T, "d": wd.d, "N": wd.N, "q_len": wd.q_len,
+               "ms_per_step": d_ms, "bound": "hbm", "achieved": dbytes / (d_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "peak": peaks["hbm_gbs"], "frac": dbytes / (d_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+               "algorithmic_bytes_per_step": dbytes, "useful_tflops": 4.0 * wd.B * wd.H * wd.d * wd.T * wd.q_len
+               / (d_ms * 1e-3) / 1e12, "launches_per_step": 2}
+        del qd, kd, vd, od, ld, wsd
+        torch.cuda.empty_cache()
+        ws = None
+
     # ---- end to end from pinned host memory (public API) --------------------
     e2e = None
     if args.e2e_steps > 0:
@@ -385,6 +422,7 @@ def main():
                       "algorithmic_bytes_per_step": mbytes, "launches_per_step": n_mrg, "ms_per_step": mrg_ms,
                       "peak_source": peaks["source"] + " hbm_gbs"},
             "fused_merge_ring": f1,
+            "decode": dec,
             "e2e": e2e,
             "gpu_launches": n_launch * args.steps,
             "cpu_baseline": cpu,

@@ -11,6 +11,8 @@ Workloads (the five shapes the library is measured and checked on):
   page1_causal_bf16    B=8 H=64 T=32768  d=128 N=4  causal  bf16
   ragged_causal_bf16   B=1 H=32 T=100000 d=128 N=4  causal  bf16  (chunks of 25000)
   million_causal_bf16  B=1 H=8 T=1048576 d=128 N=16 causal  bf16
+  decode_million_bf16  B=4 H=8 T=1048576 d=128 N=16 shards, 1 new token per
+                       sequence against a million-token KV cache (decode)
 
 The page-1 shape is the hidden state of "Sequence parallelism -- splitting
 the token dimension across GPUs" (llmdaily day 58, section "Start with the
@@ -45,6 +47,7 @@ class Workload:
     dtype: str          # "f32" or "bf16"
     recipe: str         # "normal", "wide" or "outlier"
     check: str          # "all" rows or "sample" rows
+    q_len: int = 0      # decode: the newest q_len tokens query the whole cache (0: every token)
 
     @property
     def Tc(self) -> int:
@@ -63,6 +66,7 @@ WORKLOADS: Dict[str, Workload] = {
         Workload("page1_causal_bf16", 8, 64, 32768, 128, 4, True, "bf16", "normal", "sample"),
         Workload("ragged_causal_bf16", 1, 32, 100000, 128, 4, True, "bf16", "wide", "sample"),
         Workload("million_causal_bf16", 1, 8, 1048576, 128, 16, True, "bf16", "outlier", "sample"),
+        Workload("decode_million_bf16", 4, 8, 1048576, 128, 16, True, "bf16", "normal", "sample", q_len=1),
     ]
 }
 

@@ -35,3 +35,21 @@ def test_full_size_workload_sampled_rows(name, fused):
     ro, rl = oracle.attend_rows(q_rows, k_h, v_h, rows, w.causal)
     stats = assert_close(g_out, g_lse, ro, rl, torch.bfloat16, what=name)
     print(name, 'fused' if fused else 'merge_kernel', stats)
+
+
+def test_decode_workload_full_size():
+    # One new token per sequence against a million-token KV cache in 16 shards,
+    # in the launch configuration the benchmark times; every query row checked.
+    need_cuda()
+    w = rsa_inputs.WORKLOADS["decode_million_bf16"]
+    q, k, v = rsa_inputs.make_workload(w, seed=0, device="cuda")
+    qd = q[:, :, w.T - w.q_len:].contiguous()
+    del q
+    out, lse = rsa.decode_attn(qd, k, v, w.N, w.causal)
+    torch.cuda.synchronize()
+    rsa.check_device_error()
+    rows = np.array([[b, h, w.T - w.q_len + r] for b in range(w.B) for h in range(w.H) for r in range(w.q_len)],
+                    dtype=np.int64)
+    ro, rl = oracle.attend_rows(qd.reshape(-1, w.d).cpu(), k.cpu(), v.cpu(), rows, w.causal)
+    stats = assert_close(out.reshape(-1, w.d), lse.reshape(-1), ro, rl, torch.bfloat16, what=w.name)
+    print(w.name, stats)
