@@ -24,7 +24,8 @@ from . import _build
 
 __all__ = [
     "RsaError", "load", "library_path", "block_attn_fwd", "merge", "merge_finalize",
-    "ring_attn", "ring_attn_noalloc", "ring_attn_timed", "decode_attn", "decode_workspace_size", "ring_attn_from_host", "workspace_size", "ring_schedule",
+    "ring_attn", "ring_attn_noalloc", "ring_attn_timed", "decode_attn", "decode_workspace_size",
+    "two_pass_attn", "two_pass_workspace_size", "ring_attn_from_host", "workspace_size", "ring_schedule",
     "set_wait_limit_ns", "check_device_error", "selftest_wait_timeout", "version",
     "RSA_F32", "RSA_BF16",
 ]
@@ -71,6 +72,9 @@ _SIGS = {
                              ctypes.c_uint, _c_void_p, _c_void_p, _c_void_p, ctypes.c_size_t, _c_void_p,
                              ctypes.POINTER(_c_void_p), ctypes.POINTER(_c_void_p), ctypes.POINTER(_i32),
                              _i32, ctypes.POINTER(_i32)],
+    "rsa_two_pass_workspace_size": [_i32, _i32, _i32, _i64, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)],
+    "rsa_two_pass_attn_fwd": [_c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _i64, _i32, _i32, _i32,
+                              _c_void_p, _c_void_p, _c_void_p, ctypes.c_size_t, _c_void_p],
     "rsa_decode_workspace_size": [_i32, _i32, _i32, _i64, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_size_t)],
     "rsa_decode_attn_fwd": [_c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _i64, _i32, _i32, _i32, _i32,
                             _c_void_p, _c_void_p, _c_void_p, ctypes.c_size_t, _c_void_p],
@@ -353,6 +357,30 @@ def ring_attn_from_host(q_host, k_host, v_host, N: int, causal: bool, device=Non
             ev_out.append(ev)
     main.wait_event(ev_out[-1])
     return b["out_host"], b["lse_host"], b
+
+
+def two_pass_workspace_size(dtype: torch.dtype, B: int, H: int, T: int, d: int, N: int) -> int:
+    n = ctypes.c_size_t(0)
+    dt = RSA_F32 if dtype == torch.float32 else RSA_BF16
+    _call("rsa_two_pass_workspace_size", dt, B, H, T, d, N, ctypes.byref(n))
+    return int(n.value)
+
+
+def two_pass_attn(q, k, v, N: int, causal: bool, out=None, lse=None, workspace=None,
+                  stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Two-pass Ring Self-Attention (full score rows per query chunk, then
+    softmax, then the value ring): (out [B, H, T, d], lse [B, H, T])."""
+    B, H, T, d = _check_qkv(q, k, v)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(two_pass_workspace_size(q.dtype, B, H, T, d, N), dtype=torch.uint8, device=q.device)
+    _call("rsa_two_pass_attn_fwd", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
+          int(bool(causal)), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+          workspace.numel() * workspace.element_size(), _stream(stream))
+    return out, lse
 
 
 def decode_workspace_size(dtype: torch.dtype, B: int, H: int, T: int, d: int, q_len: int, N: int) -> int:

@@ -429,6 +429,58 @@ rsa_status check_decode(rsa_dtype dt, int B, int H, int64_t T, int d, int q_len,
 
 extern "C" {
 
+static rsa_status check_two_pass(rsa_dtype dt, int B, int H, int64_t T, int d, int N)
+{
+    RSA_TRY(check_shape(dt, B, H, T, d));
+    if (N < 1 || N > T || T % N != 0)
+        return fail(RSA_ERR_INVALID_ARG, "N=%d must be >= 1 and divide T=%lld", N, (long long)T);
+    if (dt != RSA_BF16 || d != 128)
+        return fail(RSA_ERR_UNSUPPORTED, "two-pass attention is built for bf16 with d = 128");
+    if ((T / N) % 128 != 0)
+        return fail(RSA_ERR_UNSUPPORTED, "two-pass attention needs chunks T/N that are a multiple of 128");
+    if ((int64_t)B * H > 65535 || T / 128 > 65535)
+        return fail(RSA_ERR_UNSUPPORTED, "two-pass attention grid too large");
+    return RSA_OK;
+}
+
+rsa_status rsa_two_pass_workspace_size(rsa_dtype dt, int B, int H, int64_t T, int d, int N, size_t *bytes)
+{
+    if (!bytes)
+        return fail(RSA_ERR_INVALID_ARG, "bytes is NULL");
+    RSA_TRY(check_two_pass(dt, B, H, T, d, N));
+    const size_t rows = (size_t)B * H * (size_t)(T / N);
+    *bytes = align256(rows * (size_t)T * 4) + align256(rows * (size_t)T * 2);
+    return RSA_OK;
+}
+
+rsa_status rsa_two_pass_attn_fwd(const void *q, const void *k, const void *v, rsa_dtype dt, int B, int H, int64_t T,
+                                 int d, int N, int causal, void *out, float *lse, void *workspace, size_t ws_bytes,
+                                 rsa_stream_t stream)
+{
+    RSA_TRY(check_two_pass(dt, B, H, T, d, N));
+    RSA_TRY(check_ptr(q, "q"));
+    RSA_TRY(check_ptr(k, "k"));
+    RSA_TRY(check_ptr(v, "v"));
+    RSA_TRY(check_ptr(out, "out"));
+    RSA_TRY(check_ptr(lse, "lse"));
+    RSA_TRY(check_ptr(workspace, "workspace"));
+    size_t need = 0;
+    RSA_TRY(rsa_two_pass_workspace_size(dt, B, H, T, d, N, &need));
+    if (ws_bytes < need)
+        return fail(RSA_ERR_INVALID_ARG, "workspace holds %zu bytes, %zu needed", ws_bytes, need);
+    RSA_TRY(check_device_for(dt));
+    unsigned int *err = nullptr;
+    RSA_TRY(device_error_word(&err));
+    const size_t rows = (size_t)B * H * (size_t)(T / N);
+    float *S = static_cast<float *>(workspace);
+    void *P = static_cast<char *>(workspace) + align256(rows * (size_t)T * 4);
+    cudaError_t e = launch_two_pass(q, k, v, (int64_t)B * H, T, N, causal, out, lse, S, P, g_wait_limit_ns.load(),
+                                    err, stream);
+    if (e != cudaSuccess)
+        return fail(RSA_ERR_CUDA, "two-pass launch: %s", cudaGetErrorString(e));
+    return RSA_OK;
+}
+
 rsa_status rsa_decode_workspace_size(rsa_dtype dt, int B, int H, int64_t T, int d, int q_len, int N, size_t *bytes)
 {
     if (!bytes)

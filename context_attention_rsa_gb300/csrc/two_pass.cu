@@ -1,0 +1,387 @@
+// Two-pass Ring Self-Attention on the GPU.
+//
+// Page: "Sequence Parallelism" (glossary entry, zhongzhoutan-coder terms),
+// section "How It Works": the key chunks circulate first, so each query chunk
+// n builds its full score rows S^n (L/N x L); the value chunks then circulate
+// and chunk n accumulates the weighted sums over them to produce O^n.  Softmax
+// is taken over each full row between the two passes.
+//
+// Unlike the online-softmax ring, this form materialises S^n: per query chunk
+// an fp32 [B*H, Tc, T] score buffer and a bf16 [B*H, Tc, T] probability
+// buffer -- the O(L/N * L) memory the online merge avoids.  Chunks are done one
+// after another, reusing the buffers:
+//   score kernel   S^n = Q_n K^T / sqrt(d) (tcgen05, one 128x128 tile per CTA),
+//                  causal entries set to -inf
+//   softmax kernel row max and sum over the whole row (one warp per row),
+//                  P^n = e^{s - m} / l in bf16, lse = m + ln l
+//   PV kernel      O^n = sum over key chunks in ring order (n - r) mod N of
+//                  P^n_j V_j (tcgen05, 128 rows per CTA, fp32 accumulator)
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "ptx_sm103.cuh"
+#include "rsa_internal.h"
+
+namespace rsa {
+namespace {
+
+constexpr int D = 128;
+constexpr uint32_t kBoxBytes = 128u * 128u;  // 128 rows x 128 bytes (64 bf16)
+constexpr uint32_t kTileBytes = 2 * kBoxBytes;  // 128 rows x 128 bf16
+constexpr int kThreads = 160;                   // warps 0-3 epilogue, warp 4 TMA + MMA
+
+struct TwoPassParams {
+    int64_t BH, T, Tc;
+    int n;        // query chunk
+    int N;
+    int causal;
+    float *S;              // [BH, Tc, T] fp32 scores of chunk n
+    __nv_bfloat16 *out;    // [BH, T, d]
+    uint64_t wait_limit_ns;
+    unsigned int *err;
+};
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
+// S^n tile (qt, kt): 128 query rows of chunk n against keys kt*128 .. +127.
+__global__ void __launch_bounds__(kThreads)
+    score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ TwoPassParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *g = smem_raw + (base - raw);
+    const uint32_t sQ = base, sK = base + kTileBytes, bar_ld = base + 2 * kTileBytes, bar_mma = bar_ld + 8;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(g + 2 * kTileBytes + 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(g + 2 * kTileBytes + 20);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = blockIdx.x, kt = blockIdx.y, bh = blockIdx.z;
+    const int64_t qrow0 = (int64_t)p.n * p.Tc + (int64_t)qt * 128;  // global position of the tile's row 0
+    const int64_t k0 = (int64_t)kt * 128;
+    const bool all_masked = p.causal && k0 > qrow0 + 127;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar_ld, 1);
+        ptx::mbar_init(bar_mma, 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 4) {
+        ptx::tmem_alloc(ptx::smem_u32(tslot), 128);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 4) {
+        if (lane == 0 && !all_masked) {
+            ptx::mbar_arrive_expect_tx(bar_ld, 2 * kTileBytes);
+            for (int b = 0; b < 2; ++b) {
+                ptx::tma_load_3d(sQ + b * kBoxBytes, &tm_q, bar_ld, b * 64, (int)qrow0, (int)bh);
+                ptx::tma_load_3d(sK + b * kBoxBytes, &tm_k, bar_ld, b * 64, (int)k0, (int)bh);
+            }
+            if (ptx::mbar_wait(bar_ld, 0, p.wait_limit_ns, abort_flag, p.err, 40)) {
+                const uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false);
+                const uint64_t dq = ptx::smem_desc_sw128(sQ, 16, 1024), dk = ptx::smem_desc_sw128(sK, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+                    ptx::mma_ss(tmem, dq + off, dk + off, idesc, kk > 0);
+                }
+                ptx::mma_commit(bar_mma);
+                volatile int no_abort = 0;
+                ptx::mbar_wait(bar_mma, 0, p.wait_limit_ns, &no_abort, p.err, 41);
+            } else {
+                volatile int no_abort = 0;  // let the copies land before the CTA exits
+                ptx::mbar_wait(bar_ld, 0, p.wait_limit_ns, &no_abort, p.err, 42);
+            }
+        }
+        __syncwarp();
+    } else {
+        const int row = warp * 32 + lane;
+        const int64_t qpos = qrow0 + row;
+        bool ok = true;
+        if (!all_masked) {
+            ok = ptx::mbar_wait(bar_mma, 0, p.wait_limit_ns, abort_flag, p.err, 43);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+            ptx::tc_fence_after();
+            const float scale = 1.0f / sqrtf((float)D);
+            const bool valid = (int64_t)qt * 128 + row < p.Tc;
+            float *dst = p.S + ((int64_t)bh * p.Tc + (int64_t)qt * 128 + row) * p.T + k0;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t s[32];
+                if (!all_masked) {
+                    ptx::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c * 32, s);
+                    ptx::tmem_ld_wait(s);
+                }
+                if (valid) {
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int64_t key = k0 + c * 32 + i;
+                        const bool masked = all_masked || (p.causal && key > qpos);
+                        v[i] = masked ? -INFINITY : u2f(s[i]) * scale;
+                    }
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                }
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 128);
+    }
+}
+
+// Softmax over each full score row of chunk n (one warp per row): P = e^{s-m}/l
+// in bf16, lse = m + ln l into the output lse.
+__global__ void __launch_bounds__(256)
+    softmax_rows_kernel(const float *__restrict__ S, __nv_bfloat16 *__restrict__ P, float *__restrict__ lse,
+                        int64_t BH, int64_t Tc, int64_t T, int n)
+{
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= BH * Tc)
+        return;
+    const float4 *src = reinterpret_cast<const float4 *>(S + row * T);
+    const int64_t n4 = T / 4;
+    // online max and sum over the lane's elements
+    float m = -INFINITY, l = 0.f;
+    for (int64_t i = lane; i < n4; i += 32) {
+        const float4 x = src[i];
+        const float mx = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+        const float mn = fmaxf(m, mx);
+        if (mn > -INFINITY) {
+            l = l * expf(m - mn) + expf(x.x - mn) + expf(x.y - mn) + expf(x.z - mn) + expf(x.w - mn);
+            m = mn;
+        }
+    }
+    float M = m;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float lw = (m > -INFINITY) ? l * expf(m - M) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        lw += __shfl_xor_sync(0xffffffffu, lw, o);
+    const bool empty = !(lw > 0.f);
+    const float inv = empty ? 0.f : 1.f / lw;
+    uint2 *dst = reinterpret_cast<uint2 *>(P + row * T);
+    for (int64_t i = lane; i < n4; i += 32) {
+        const float4 x = src[i];
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+        if (!empty) {
+            e[0] = expf(x.x - M) * inv;
+            e[1] = expf(x.y - M) * inv;
+            e[2] = expf(x.z - M) * inv;
+            e[3] = expf(x.w - M) * inv;
+        }
+        __nv_bfloat162 a = __floats2bfloat162_rn(e[0], e[1]), b = __floats2bfloat162_rn(e[2], e[3]);
+        dst[i] = make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
+    }
+    if (lane == 0) {
+        const int64_t bh = row / Tc, r = row - bh * Tc;
+        lse[bh * T + (int64_t)n * Tc + r] = empty ? -INFINITY : M + logf(lw);
+    }
+}
+
+// O^n rows qt*128.. of head bh: sum over key chunks j in ring order (n - r) mod N
+// of P^n_j V_j, 128 keys per step, two shared-memory stages.
+__global__ void __launch_bounds__(kThreads)
+    pv_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_v,
+              const __grid_constant__ TwoPassParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *g = smem_raw + (base - raw);
+    // stage s: P tile at base + s*2*kTileBytes, V tile right after it
+    const uint32_t bars = base + 4 * kTileBytes;  // full[2], empty[2], done
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(g + 4 * kTileBytes + 48);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(g + 4 * kTileBytes + 52);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = blockIdx.x, bh = blockIdx.y;
+    const int64_t tiles_per_chunk = p.Tc / 128;
+    const int chunks = p.causal ? p.n + 1 : p.N;  // causal: chunks after n are all zero
+    const int64_t nt = tiles_per_chunk * chunks;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 5; ++i)
+            ptx::mbar_init(bars + 8 * i, 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 4) {
+        ptx::tmem_alloc(ptx::smem_u32(tslot), 128);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tslot;
+    auto FULL = [&](int s) { return bars + 8u * s; };
+    auto EMPTY = [&](int s) { return bars + 16u + 8u * s; };
+    const uint32_t DONE = bars + 32u;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            // key tile i: ring round r = i / tiles_per_chunk visits chunk (n - r) mod N
+            auto key0 = [&](int64_t i) -> int64_t {
+                const int64_t r = i / tiles_per_chunk;
+                const int64_t j = ((p.n - r) % p.N + p.N) % p.N;
+                return j * p.Tc + (i - r * tiles_per_chunk) * 128;
+            };
+            auto load = [&](int64_t i) {
+                const int s = (int)(i & 1);
+                const uint32_t sp = base + s * 2 * kTileBytes, sv = sp + kTileBytes;
+                const int64_t kk0 = key0(i);
+                ptx::mbar_arrive_expect_tx(FULL(s), 2 * kTileBytes);
+                for (int b = 0; b < 2; ++b) {
+                    ptx::tma_load_3d(sp + b * kBoxBytes, &tm_p, FULL(s), (int)(kk0 + b * 64), qt * 128, (int)bh);
+                    ptx::tma_load_3d(sv + b * kBoxBytes, &tm_v, FULL(s), b * 64, (int)kk0, (int)bh);
+                }
+            };
+            const uint32_t idesc = ptx::idesc_bf16_f32(128, D, true);
+            const uint64_t dp0 = ptx::smem_desc_sw128(base, 16, 1024);
+            const uint64_t dv0 = ptx::smem_desc_sw128(base + kTileBytes, kBoxBytes, 1024);
+            bool ok = true;
+            int64_t issued = 0;
+            if (nt > 0) {
+                load(0);
+                issued = 1;
+            }
+            for (int64_t i = 0; ok && i < nt; ++i) {
+                if (i + 1 < nt) {
+                    if (i + 1 >= 2)
+                        ok = ptx::mbar_wait(EMPTY((int)((i + 1) & 1)), (uint32_t)(((i + 1) / 2 - 1) & 1),
+                                            p.wait_limit_ns, abort_flag, p.err, 50);
+                    if (!ok)
+                        break;
+                    load(i + 1);
+                    issued = i + 2;
+                }
+                const int s = (int)(i & 1);
+                ok = ptx::mbar_wait(FULL(s), (uint32_t)((i / 2) & 1), p.wait_limit_ns, abort_flag, p.err, 51);
+                if (!ok)
+                    break;
+                const uint64_t pa = dp0 + ((s * 2 * kTileBytes) >> 4);
+                const uint64_t vb = dv0 + ((s * 2 * kTileBytes) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+                    ptx::mma_ss(tmem, pa + off, vb + ((kk * 2048) >> 4), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                ptx::mma_commit(EMPTY(s));
+            }
+            ptx::mma_commit(DONE);
+            volatile int no_abort = 0;
+            ptx::mbar_wait(DONE, 0, p.wait_limit_ns, &no_abort, p.err, 52);
+            // copies still in flight after an abort land before the CTA exits
+            for (int64_t i = (issued > 2 ? issued - 2 : 0); i < issued; ++i)
+                ptx::mbar_wait(FULL((int)(i & 1)), (uint32_t)((i / 2) & 1), p.wait_limit_ns, &no_abort, p.err, 53);
+        }
+        __syncwarp();
+    } else {
+        const int row = warp * 32 + lane;
+        bool ok = ptx::mbar_wait(DONE, 0, p.wait_limit_ns, abort_flag, p.err, 54);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+            ptx::tc_fence_after();
+            const bool valid = (int64_t)qt * 128 + row < p.Tc;
+            __nv_bfloat16 *dst = p.out + ((int64_t)bh * p.T + (int64_t)p.n * p.Tc + (int64_t)qt * 128 + row) * D;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t o[32];
+                if (nt > 0) {
+                    ptx::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c * 32, o);
+                    ptx::tmem_ld_wait(o);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        o[i] = 0u;
+                }
+                if (valid) {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        __nv_bfloat162 h[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            h[e] = __floats2bfloat162_rn(u2f(o[8 * i + 2 * e]), u2f(o[8 * i + 2 * e + 1]));
+                        d4[i] = make_uint4(*reinterpret_cast<uint32_t *>(&h[0]), *reinterpret_cast<uint32_t *>(&h[1]),
+                                           *reinterpret_cast<uint32_t *>(&h[2]), *reinterpret_cast<uint32_t *>(&h[3]));
+                    }
+                }
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 128);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_two_pass(const void *q, const void *k, const void *v, int64_t BH, int64_t T, int N, int causal,
+                            void *out, float *lse, float *S, void *P, uint64_t wait_limit_ns, unsigned int *err,
+                            cudaStream_t s)
+{
+    const int64_t Tc = T / N;
+    CUtensorMap mq, mk, mv, mp;
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)T, (uint64_t)BH};
+    const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)T * D * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    const uint64_t pdims[3] = {(uint64_t)T, (uint64_t)Tc, (uint64_t)BH};
+    const uint64_t pstrides[2] = {(uint64_t)T * 2, (uint64_t)Tc * T * 2};
+    if (!make_bf16_map_sw128(&mq, q, 3, dims, strides, box) || !make_bf16_map_sw128(&mk, k, 3, dims, strides, box) ||
+        !make_bf16_map_sw128(&mv, v, 3, dims, strides, box) || !make_bf16_map_sw128(&mp, P, 3, pdims, pstrides, box))
+        return cudaErrorInvalidValue;
+    const uint32_t smem_score = 2 * kTileBytes + 64 + 1024, smem_pv = 4 * kTileBytes + 64 + 1024;
+    cudaError_t e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_score);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(pv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_pv);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t n_qt = (Tc + 127) / 128, n_kt = T / 128;
+    if (BH > 65535 || n_kt > 65535)
+        return cudaErrorInvalidConfiguration;
+    for (int n = 0; n < N; ++n) {
+        TwoPassParams p;
+        p.BH = BH;
+        p.T = T;
+        p.Tc = Tc;
+        p.n = n;
+        p.N = N;
+        p.causal = causal ? 1 : 0;
+        p.S = S;
+        p.out = static_cast<__nv_bfloat16 *>(out);
+        p.wait_limit_ns = wait_limit_ns;
+        p.err = err;
+        score_kernel<<<dim3((unsigned)n_qt, (unsigned)n_kt, (unsigned)BH), kThreads, smem_score, s>>>(mq, mk, p);
+        const int64_t rows = BH * Tc;
+        softmax_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(S, static_cast<__nv_bfloat16 *>(P), lse, BH,
+                                                                       Tc, T, n);
+        pv_kernel<<<dim3((unsigned)n_qt, (unsigned)BH), kThreads, smem_pv, s>>>(mp, mv, p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace rsa

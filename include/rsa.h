@@ -215,6 +215,26 @@ rsa_status rsa_decode_attn_fwd(const void *q, const void *k, const void *v, rsa_
                                rsa_stream_t stream);
 
 /*
+ * Two-pass Ring Self-Attention ([P3] "How It Works", steps 1-2), the form that
+ * keeps whole score rows: for each query chunk n in turn, the score pass
+ * visits the key chunks in ring order (n - r) mod N and fills the full score
+ * rows S^n = Q_n K^T / sqrt(d) (future keys -inf when causal); softmax is
+ * taken over each full row (lse = log-sum-exp of the row); the output pass
+ * visits the value chunks in the same ring order and accumulates
+ * O^n = sum_j P^n_j V_j in fp32.  Same inputs and outputs as
+ * rsa_ring_attn_fwd; the workspace holds one chunk's fp32 scores and bf16
+ * probabilities, B*H*(T/N)*T*6 bytes -- the O(L/N * L) memory the online
+ * merge avoids.  Built for bf16 with d = 128 and T/N a multiple of 128
+ * (RSA_ERR_UNSUPPORTED otherwise).
+ */
+rsa_status rsa_two_pass_workspace_size(rsa_dtype dt, int B, int H, int64_t T, int d, int N,
+                                       size_t *bytes);
+rsa_status rsa_two_pass_attn_fwd(const void *q, const void *k, const void *v, rsa_dtype dt,
+                                 int B, int H, int64_t T, int d, int N, int causal,
+                                 void *out, float *lse, void *workspace, size_t ws_bytes,
+                                 rsa_stream_t stream);
+
+/*
  * Host-only view of the ring schedule used by rsa_ring_attn_fwd: the pairs of
  * round r (0-based) as (q_chunk[p], kv_chunk[p]) in host arrays of length
  * `cap`; their count goes to *n_pairs.  No GPU needed.

@@ -153,3 +153,14 @@ def test_decode_workspace_and_validation():
     assert lib.rsa_decode_attn_fwd(*bad) == 1
     bad = list(args); bad[14] = 16        # workspace too small
     assert lib.rsa_decode_attn_fwd(*bad) == 1
+
+
+def test_two_pass_workspace_is_quadratic():
+    import torch
+    B, H, T, d, N = 2, 8, 4096, 128, 4
+    ws = rsa.two_pass_workspace_size(torch.bfloat16, B, H, T, d, N)
+    assert ws == B * H * (T // N) * T * (4 + 2)
+    lib = rsa.load()
+    n = ctypes.c_size_t(0)
+    assert lib.rsa_two_pass_workspace_size(1, 1, 1, 384, 128, 2, ctypes.byref(n)) == 2  # 192-key chunks
+    assert lib.rsa_two_pass_workspace_size(0, 1, 1, 256, 128, 2, ctypes.byref(n)) == 2  # fp32
