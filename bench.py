@@ -212,6 +212,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fused", action="store_true", help="skip timing the fused-merge ring variant")
     ap.add_argument("--no-decode", action="store_true", help="skip timing decode on the million-token cache")
+    ap.add_argument("--no-two-pass", action="store_true", help="skip timing the two-pass RSA form")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--shape", default=None,
                     help="B,H,T,d,N,causal: a bf16 normal-recipe workload instead of --workload (profiling)")
@@ -359,6 +360,43 @@ def main():
         torch.cuda.empty_cache()
         ws = None
 
+    # ---- two-pass RSA (full score rows) on the bidirectional workload -------
+    tp = None
+    if not args.no_two_pass and world == 1:
+        wt = rsa_inputs.WORKLOADS["noncausal_bf16"]
+        qt, kt, vt = rsa_inputs.make_workload(wt, seed=0, device=dev)
+        ot = torch.empty_like(qt)
+        lt = torch.empty((wt.B, wt.H, wt.T), dtype=torch.float32, device=dev)
+        wst = torch.empty(rsa.two_pass_workspace_size(qt.dtype, wt.B, wt.H, wt.T, wt.d, wt.N), dtype=torch.uint8,
+                          device=dev)
+        wsr = torch.empty(max(rsa.workspace_size(qt.dtype, wt.B, wt.H, wt.T, wt.d, wt.N, wt.causal), 1),
+                          dtype=torch.uint8, device=dev)
+        timings = {}
+        for name, fn in (("two_pass", lambda: rsa.two_pass_attn(qt, kt, vt, wt.N, wt.causal, out=ot, lse=lt,
+                                                                 workspace=wst)),
+                         ("online_ring", lambda: rsa.ring_attn(qt, kt, vt, wt.N, wt.causal, out=ot, lse=lt,
+                                                               workspace=wsr))):
+            for _ in range(max(args.warmup, 0)):
+                fn()
+            torch.cuda.synchronize()
+            t0_ = torch.cuda.Event(enable_timing=True)
+            t1_ = torch.cuda.Event(enable_timing=True)
+            t0_.record(stream)
+            for _ in range(args.steps):
+                fn()
+            t1_.record(stream)
+            torch.cuda.synchronize()
+            timings[name] = t0_.elapsed_time(t1_) / args.steps
+        rsa.check_device_error()
+        fl_t = useful_flops(wt.B, wt.H, wt.T, wt.d, wt.causal)
+        tp = {"workload": wt.name, "ms_per_step": timings["two_pass"],
+              "tflops": fl_t / (timings["two_pass"] * 1e-3) / 1e12,
+              "workspace_bytes": int(wst.numel()), "online_ring_ms_per_step": timings["online_ring"],
+              "online_ring_tflops": fl_t / (timings["online_ring"] * 1e-3) / 1e12,
+              "online_ring_workspace_bytes": int(wsr.numel()), "launches_per_step": 3 * wt.N}
+        del qt, kt, vt, ot, lt, wst, wsr
+        torch.cuda.empty_cache()
+
     # ---- end to end from pinned host memory (public API) --------------------
     e2e = None
     if args.e2e_steps > 0:
@@ -423,6 +461,7 @@ def main():
                       "peak_source": peaks["source"] + " hbm_gbs"},
             "fused_merge_ring": f1,
             "decode": dec,
+            "two_pass_rsa": tp,
             "e2e": e2e,
             "gpu_launches": n_launch * args.steps,
             "cpu_baseline": cpu,
