@@ -81,6 +81,7 @@ _SIGS = {
     "rsa_ring_schedule": [_i32, _i32, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _i32,
                           ctypes.POINTER(_i32)],
     "rsa_set_wait_limit_ns": [ctypes.c_uint64],
+    "rsa_set_block_kernel": [_i32],
     "rsa_check_device_error": [_c_void_p],
     "rsa_selftest_wait_timeout": [_c_void_p],
     "rsa_status_string": [_i32],
@@ -428,6 +429,16 @@ def ring_schedule(N: int, causal: bool, rnd: int) -> List[Tuple[int, int]]:
 
 def set_wait_limit_ns(limit_ns: int) -> None:
     _call("rsa_set_wait_limit_ns", int(limit_ns))
+
+
+BLOCK_KERNELS = {"auto": 0, "one_sm": 1, "two_sm": 2}
+
+
+def set_block_kernel(which: str) -> None:
+    """Pick the bf16 tensor-core block kernel for later calls: "auto" (the
+    one-SM kernel), "one_sm", or "two_sm" (the CTA-pair kernel where it
+    applies: d = 128, pairs of at least 512 rows, no key splits)."""
+    _call("rsa_set_block_kernel", BLOCK_KERNELS[which])
 
 
 def check_device_error(stream=None) -> None:

@@ -34,13 +34,16 @@
 
 #include "ptx_sm103.cuh"
 #include "rsa_internal.h"
+#include "tc_common.cuh"
+#include "tc_softmax.cuh"
 
 namespace rsa {
 namespace {
 
+using namespace tc;
+
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 256x
 
 template <int D>
 struct Cfg {
@@ -65,52 +68,6 @@ struct Cfg {
     static constexpr int kNumBars = kDrain + 1;
     static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
 };
-
-__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
-__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
-{
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
-__device__ __forceinline__ float fmax3(float a, float b, float c)
-{
-    float r;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-    return r;
-}
-
-// Named barrier 1 over the 256 softmax threads (warps 0-7).
-__device__ __forceinline__ void softmax_bar_sync()
-{
-    asm volatile("barrier.cta.sync 1, 256;" ::: "memory");
-}
-
-// The same barrier, returning whether `v` holds in every softmax thread, so
-// that a decision to give up is taken by all of them together.
-__device__ __forceinline__ bool softmax_bar_and(bool v)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "barrier.cta.red.and.pred po, 1, 256, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-}
-
-// Keep uses of r[0..31] after a preceding volatile asm (the TMEM load wait).
-__device__ __forceinline__ void tie32(uint32_t *r)
-{
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-        asm volatile("" : "+r"(r[i]));
-}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -248,6 +205,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < 8; ++kk)
                     ptx::mma_ts(dst, pa + kk * 8, vb + ((kk * 2048) >> 4), idesc_pv, (acc || kk > 0) ? 1u : 0u);
             };
+            // P_t(j) complete (every softmax thread arrived): O_t += P_t V_j.
+            auto pv_tile = [&](int t, int slot, int j) -> bool {
+                if (!ptx::mbar_wait(BAR(C::kPF + t), j & 1, lim_ns, abort_flag, p.err, 13 + 2 * t))
+                    return false;
+                ptx::tc_fence_after();
+                issue_pv(t, slot, j > 0);
+                return true;
+            };
             bool ok = ptx::mbar_wait(BAR(C::kQF), 0, lim_ns, abort_flag, p.err, 10);
             int kslot = 0;
             if (ok)
@@ -266,11 +231,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok)
                     break;
                 // tile 0
-                ok = ptx::mbar_wait(BAR(C::kPF + 0), j & 1, lim_ns, abort_flag, p.err, 13);
+                ok = pv_tile(0, vslot, j);
                 if (!ok)
                     break;
-                ptx::tc_fence_after();
-                issue_pv(0, vslot, j > 0);
                 const bool more = j + 1 < n;
                 if (more) {
                     const int kld = 2 * (j + 1);
@@ -285,11 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_commit(BAR(C::kOF + 0));
                 }
                 // tile 1
-                ok = ptx::mbar_wait(BAR(C::kPF + 1), j & 1, lim_ns, abort_flag, p.err, 15);
+                ok = pv_tile(1, vslot, j);
                 if (!ok)
                     break;
-                ptx::tc_fence_after();
-                issue_pv(1, vslot, j > 0);
                 ptx::mma_commit(BAR(C::kKVE + vslot));
                 if (more) {
                     issue_qk(1, kslot);
@@ -307,218 +268,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ============================== softmax ==============================
-        // All eight warps work on tile 0's S, then on tile 1's (the tiles
-        // alternate on the tensor cores).  Two threads share a row: warp w
-        // holds TMEM lanes 32*(w%4).. and column half h = w/4, i.e. keys
-        // [64h, 64h+64) of every 128-key step and output columns
-        // [h*d/2, (h+1)*d/2).  The two halves of a row agree on the row max
-        // through shared memory; each keeps its own part of the row sum.
-        const int h = warp >> 2;
-        const int wi = warp & 3;
-        const int row = wi * 32 + lane;
-        const uint32_t lane_addr = (uint32_t)(wi * 32) << 16;
-        float *xch = reinterpret_cast<float *>(gbase + C::kXchOff);  // [tile][half][row]
-        const float sl2 = 1.4426950408889634f / sqrtf((float)D);   // log2(e) / sqrt(d)
-        float m_used[2] = {-INFINITY, -INFINITY};                    // kept maxima, log2 units
-        float l[2] = {0.f, 0.f};                                     // this half's row sums
-        int64_t allowed[2];  // keys [0, allowed) of this split visible to the row, per tile
+        SoftmaxCtx ctx;
+        ctx.tmem = tmem;
+        ctx.col_s[0] = C::kColS0;
+        ctx.col_s[1] = C::kColS1;
+        ctx.col_o[0] = C::kColO0;
+        ctx.col_o[1] = C::kColO1;
         for (int t = 0; t < 2; ++t) {
-            const int64_t qpos = pr.q_off + q0 + t * 128 + row;
-            allowed[t] = p.causal ? min(kv_len, qpos - kv_off + 1) : kv_len;
+            ctx.bar_sf[t] = BAR(C::kSF + t);
+            ctx.bar_of[t] = BAR(C::kOF + t);
         }
-        bool ok = true;
-        for (int j = 0; ok && j < n; ++j) {
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const uint32_t tS = tmem + lane_addr + (t ? C::kColS1 : C::kColS0);
-                const uint32_t tO = tmem + lane_addr + (t ? C::kColO1 : C::kColO0);
-                bool got = ptx::mbar_wait(BAR(C::kSF + t), j & 1, lim_ns, abort_flag, p.err, 20);
-                got = __all_sync(0xffffffffu, got);
-                uint32_t s[64];
-                float mx = -INFINITY;
-                if (got) {
-                    ptx::tc_fence_after();
-                    ptx::tmem_ld32(tS + 64 * h, s);
-                    ptx::tmem_ld32(tS + 64 * h + 32, s + 32);
-                    ptx::tmem_ld_wait(s);
-                    tie32(s + 32);
-                    const int64_t lim = allowed[t] - (int64_t)j * 128 - 64 * h;
-                    if (lim < 64) {
-#pragma unroll
-                        for (int i = 0; i < 64; ++i)
-                            if ((int64_t)i >= lim)
-                                s[i] = f2u(-INFINITY);
-                    }
-                    // row max of this half: four independent chains of three-input max
-                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                    for (int i = 0; i < 64; i += 8) {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            m4[c] = fmax3(m4[c], u2f(s[i + 2 * c]), u2f(s[i + 2 * c + 1]));
-                    }
-                    mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
-                    xch[(t * 2 + h) * 128 + row] = mx;
-                }
-                // Every S load of this tile is done (and every thread knows
-                // whether all waits succeeded) before any half writes P over S.
-                ptx::tc_fence_before();
-                ok = softmax_bar_and(got);
-                ptx::tc_fence_after();
-                if (!ok)
-                    break;
-                mx = fmaxf(mx, xch[(t * 2 + (h ^ 1)) * 128 + row]);
-                const float mnew = mx * sl2;
-                const bool need =
-                    (mnew > -INFINITY) && (m_used[t] == -INFINITY || mnew > m_used[t] + kRescaleThreshold);
-                if (__any_sync(0xffffffffu, need)) {
-                    float alpha = 1.f;
-                    if (need) {
-                        alpha = (m_used[t] == -INFINITY) ? 0.f : ptx::ex2(m_used[t] - mnew);
-                        l[t] *= alpha;
-                        m_used[t] = mnew;
-                    }
-                    if (j > 0) {
-                        // the commit that signalled S_t(j) also covered PV_t(j-1): O_t is stable
-                        const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll 1
-                        for (int c = 0; c < D / 64; ++c) {
-                            uint32_t o[32];
-                            const uint32_t ta = tO + h * (D / 2) + c * 32;
-                            ptx::tmem_ld32(ta, o);
-                            ptx::tmem_ld_wait(o);
-#pragma unroll
-                            for (int i = 0; i < 32; i += 2) {
-                                const float2 r = __fmul2_rn(make_float2(u2f(o[i]), u2f(o[i + 1])), a2);
-                                o[i] = f2u(r.x);
-                                o[i + 1] = f2u(r.y);
-                            }
-                            ptx::tmem_st32(ta, o);
-                        }
-                    }
-                }
-                // p = 2^(s * log2(e)/sqrt(d) - m), written over S as bf16 pairs:
-                // keys [64h, 64h+64) are packed columns [32h, 32h+32)
-                const float neg = (m_used[t] == -INFINITY) ? 0.f : -m_used[t];
-                const float2 c2 = make_float2(sl2, sl2);
-                const float2 n2 = make_float2(neg, neg);
-                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                                 make_float2(0.f, 0.f)};
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float2 x = __ffma2_rn(make_float2(u2f(s[2 * i]), u2f(s[2 * i + 1])), c2, n2);
-                    const float p0 = ptx::ex2(x.x);
-                    const float p1 = ptx::ex2(x.y);
-                    acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
-                    pk[i] = pack_bf16(p0, p1);
-                }
-                ptx::tmem_st32(tS + 32 * h, pk);
-                const float2 a01 = __fadd2_rn(acc[0], acc[1]);
-                const float2 a23 = __fadd2_rn(acc[2], acc[3]);
-                const float2 a = __fadd2_rn(a01, a23);
-                l[t] += a.x + a.y;
-                ptx::tmem_st_wait();
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(BAR(C::kPF + t));
-            }
-        }
-        // ---- epilogue: O / l and lse for both tiles --------------------------------
-        bool fin = ok;
-        for (int t = 0; t < 2 && fin && n > 0; ++t) {
-            fin = ptx::mbar_wait(BAR(C::kOF + t), 0, lim_ns, abort_flag, p.err, 21);
-            fin = __all_sync(0xffffffffu, fin);
-        }
-        softmax_bar_sync();  // the exchange slots are free again
-        if (ok) {
-            xch[(0 * 2 + h) * 128 + row] = l[0];
-            xch[(1 * 2 + h) * 128 + row] = l[1];
-        }
-        fin = softmax_bar_and(fin && ok);
-        if (fin) {
-            ptx::tc_fence_after();
-#pragma unroll 1
-            for (int t = 0; t < 2; ++t) {
-                const float lt = l[t] + xch[(t * 2 + (h ^ 1)) * 128 + row];
-                const uint32_t tO = tmem + lane_addr + (t ? C::kColO1 : C::kColO0);
-                const int64_t rg = q0 + t * 128 + row;  // row inside the pair
-                const bool valid = rg < p.q_len;
-                const int64_t orow = (int64_t)bh * pr.out_T + pr.out_t0 + rg + (int64_t)sp * pr.split_stride;
-                // This pair's result is (O / l, lse_b).  A merging epilogue folds it
-                // into the running (acc, lse) as the merge kernel does:
-                // M = max(a, b), L = M + ln(e^{a-M} + e^{b-M}), o = acc e^{a-L} + o_b e^{b-L}.
-                const bool empty = !(lt > 0.f);
-                const float lse_b = empty ? -INFINITY : (m_used[t] + ptx::lg2(lt)) * 0.69314718055994531f;
-                float wa = 0.f;                     // weight of the accumulator row
-                float wb = empty ? 0.f : 1.f / lt;  // weight of the unnormalised O row
-                float lse_out = lse_b;
-                const bool merging = pr.mode != kStore;
-                if (merging && valid) {
-                    const float a = pr.lse[orow];
-                    const float M = fmaxf(a, lse_b);
-                    if (M > -INFINITY) {
-                        const float ea = ptx::ex2((a - M) * 1.4426950408889634f);
-                        const float eb = ptx::ex2((lse_b - M) * 1.4426950408889634f);
-                        const float tot = ea + eb;
-                        const float inv = 1.f / tot;
-                        lse_out = M + ptx::lg2(tot) * 0.69314718055994531f;
-                        wa = ea * inv;
-                        wb = empty ? 0.f : eb * inv / lt;
-                    } else {
-                        lse_out = -INFINITY;
-                        wb = 0.f;
-                    }
-                }
-                softmax_bar_sync();  // both halves have read the running lse
-                if (valid && h == 0)
-                    pr.lse[orow] = lse_out;
-#pragma unroll 1
-                for (int c = 0; c < D / 64; ++c) {
-                    const int col = h * (D / 2) + c * 32;  // first output column of this chunk
-                    uint32_t o[32];
-                    if (n > 0) {
-                        ptx::tmem_ld32(tO + col, o);
-                        ptx::tmem_ld_wait(o);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            o[i] = 0u;
-                    }
-                    if (valid) {
-                        float v[32];
-                        if (merging) {
-                            const float4 *src = reinterpret_cast<const float4 *>(pr.acc + orow * D + col);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const float4 x = src[i];
-                                v[4 * i] = fmaf(u2f(o[4 * i]), wb, x.x * wa);
-                                v[4 * i + 1] = fmaf(u2f(o[4 * i + 1]), wb, x.y * wa);
-                                v[4 * i + 2] = fmaf(u2f(o[4 * i + 2]), wb, x.z * wa);
-                                v[4 * i + 3] = fmaf(u2f(o[4 * i + 3]), wb, x.w * wa);
-                            }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                v[i] = u2f(o[i]) * wb;
-                        }
-                        if (pr.out_f32) {
-                            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(pr.out) + orow * D + col);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                        } else {
-                            uint4 *dst =
-                                reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.out) + orow * D + col);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                dst[i] = make_uint4(pack_bf16(v[8 * i], v[8 * i + 1]), pack_bf16(v[8 * i + 2], v[8 * i + 3]),
-                                                    pack_bf16(v[8 * i + 4], v[8 * i + 5]),
-                                                    pack_bf16(v[8 * i + 6], v[8 * i + 7]));
-                        }
-                    }
-                }
-            }
-        }
+        ctx.xch = reinterpret_cast<float *>(gbase + C::kXchOff);
+        ctx.abort_flag = abort_flag;
+        ctx.lim_ns = lim_ns;
+        softmax_warps<D>(ctx, p, pr, q0, n, kv_off, kv_len, bh, (int64_t)sp * pr.split_stride,
+                         [&](int t) { ptx::mbar_arrive(BAR(C::kPF + t)); });
     }
 
     // ---- teardown --------------------------------------------------------------
@@ -565,6 +329,8 @@ cudaError_t launch_d(const void *q, const void *k, const void *v, const BlockPar
 cudaError_t launch_block_attn_bf16(const void *q, const void *k, const void *v, const BlockParams &p,
                                    cudaStream_t s)
 {
+    if (p.tc_kernel == 2 && block_attn_2sm_applies(p))
+        return launch_block_attn_bf16_2sm(q, k, v, p, s);
     if (p.d == 128)
         return launch_d<128>(q, k, v, p, s);
     if (p.d == 64)

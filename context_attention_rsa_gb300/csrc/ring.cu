@@ -46,6 +46,7 @@ namespace {
 __device__ unsigned int g_device_error;
 
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int> g_tc_kernel{0};
 
 constexpr int kMaxDevices = 64;
 
@@ -250,6 +251,7 @@ BlockParams base_params(rsa_dtype dt, int B, int H, int64_t T, int d, int causal
     p.n_split = 1;
     p.n_qgroups = (int)((q_len + kBf16RowsPerCta - 1) / kBf16RowsPerCta);
     p.wait_limit_ns = g_wait_limit_ns.load();
+    p.tc_kernel = g_tc_kernel.load();
     p.err = err;
     (void)dt;
     return p;
@@ -721,6 +723,14 @@ rsa_status rsa_set_wait_limit_ns(uint64_t limit_ns)
     if (limit_ns < 1000000ull)
         return fail(RSA_ERR_INVALID_ARG, "wait limit must be >= 1 ms");
     g_wait_limit_ns.store(limit_ns);
+    return RSA_OK;
+}
+
+rsa_status rsa_set_block_kernel(int which)
+{
+    if (which < RSA_BLOCK_KERNEL_AUTO || which > RSA_BLOCK_KERNEL_TWO_SM)
+        return fail(RSA_ERR_INVALID_ARG, "block kernel choice %d is not 0, 1 or 2", which);
+    g_tc_kernel.store(which);
     return RSA_OK;
 }
 

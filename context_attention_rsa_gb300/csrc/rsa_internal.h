@@ -54,6 +54,7 @@ struct BlockParams {
     int npairs;
     int n_qgroups;          // query-row groups per pair (rows per CTA granularity)
     uint64_t wait_limit_ns;
+    int tc_kernel;          // tensor-core kernel choice: 0 automatic (one-SM), 1 one-SM, 2 two-SM where it applies
     unsigned int *err;      // device error word
     PairDesc pairs[kMaxPairsPerLaunch];
 };
@@ -105,6 +106,15 @@ bool make_bf16_map_sw128(CUtensorMap *m, const void *ptr, int rank, const uint64
 
 // Rows of one CTA of the tensor-core kernel (two 128-row tiles).
 constexpr int kBf16RowsPerCta = 256;
+// Rows of one CTA pair of the two-SM tensor-core kernel.
+constexpr int kBf16RowsPerCluster = 512;
+
+// The two-SM kernel serves d = 128 launches without key splits whose pairs
+// have at least one full cluster of rows; launch_block_attn_bf16 picks it for
+// those when BlockParams::tc_kernel asks for it (2), else the one-SM kernel.
+bool block_attn_2sm_applies(const BlockParams &p);
+cudaError_t launch_block_attn_bf16_2sm(const void *q, const void *k, const void *v, const BlockParams &p,
+                                       cudaStream_t s);
 
 // Set the thread's last-error text and return `st`.
 rsa_status fail(rsa_status st, const char *fmt, ...);

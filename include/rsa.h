@@ -246,6 +246,24 @@ rsa_status rsa_ring_schedule(int N, int causal, int round, int *q_chunk, int *kv
 rsa_status rsa_set_wait_limit_ns(uint64_t limit_ns);
 
 /*
+ * Which bf16 tensor-core kernel computes the blocks of later calls (process
+ * wide).  Both give the result of rsa_block_attn_fwd; they differ in how the
+ * work is laid out on the GPU:
+ *   RSA_BLOCK_KERNEL_ONE_SM  one CTA per 256 query rows of a (pair, head);
+ *   RSA_BLOCK_KERNEL_TWO_SM  one pair of CTAs (a two-CTA cluster) per 512
+ *                            rows, sharing each K/V tile through the paired
+ *                            (cta_group::2) MMA; used for d = 128 when a
+ *                            pair has at least 512 query rows and its key
+ *                            range is not split (not the decode path);
+ *   RSA_BLOCK_KERNEL_AUTO    (default) the one-SM kernel, measured the
+ *                            faster of the two on every workload this
+ *                            library is benchmarked on.
+ * Returns RSA_ERR_INVALID_ARG for any other value.  Host only.
+ */
+enum { RSA_BLOCK_KERNEL_AUTO = 0, RSA_BLOCK_KERNEL_ONE_SM = 1, RSA_BLOCK_KERNEL_TWO_SM = 2 };
+rsa_status rsa_set_block_kernel(int which);
+
+/*
  * Synchronise `stream`, then read and clear the device error word of the
  * current device: RSA_OK, or RSA_ERR_TIMEOUT if a kernel gave up on a wait.
  */

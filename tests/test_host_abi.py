@@ -164,3 +164,11 @@ def test_two_pass_workspace_is_quadratic():
     n = ctypes.c_size_t(0)
     assert lib.rsa_two_pass_workspace_size(1, 1, 1, 384, 128, 2, ctypes.byref(n)) == 2  # 192-key chunks
     assert lib.rsa_two_pass_workspace_size(0, 1, 1, 256, 128, 2, ctypes.byref(n)) == 2  # fp32
+
+
+def test_set_block_kernel_accepts_the_three_choices_only():
+    lib = rsa.load()
+    assert lib.rsa_set_block_kernel(3) == 1
+    assert lib.rsa_set_block_kernel(-1) == 1
+    for which in (1, 2, 0):
+        assert lib.rsa_set_block_kernel(which) == 0
