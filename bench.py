@@ -412,11 +412,14 @@ def main():
         e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
         barrier()
         torch.cuda.synchronize()
+        e_clocks = ClockSampler(local)
+        time.sleep(0.3)
         e_ev[0].record(stream)
         for i in range(args.e2e_steps):
             rsa.ring_attn_from_host(qh, kh, vh, N, causal, device=dev, buffers=bufs)
             e_ev[i + 1].record(stream)
         torch.cuda.synchronize()
+        e_clk = e_clocks.stop()
         barrier()
         e_steps = [e_ev[i].elapsed_time(e_ev[i + 1]) for i in range(args.e2e_steps)]
         e_ms = sum(e_steps) / args.e2e_steps
@@ -427,7 +430,7 @@ def main():
         h2d = 3 * qh.numel() * qh.element_size()
         d2h = bufs["out_host"].numel() * bufs["out_host"].element_size() + bufs["lse_host"].numel() * 4
         e2e = {"value": flops * world / (e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
-               "step_ms": [round(x, 2) for x in e_steps],
+               "step_ms": [round(x, 2) for x in e_steps], "clocks": e_clk,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         k_cpu, v_cpu, q_cpu = kh, vh, qh
     else:
