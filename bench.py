@@ -153,8 +153,11 @@ def cpu_baseline(w, q_cpu_rows, k_cpu, v_cpu, rows, budget_s=15.0):
     oracle.attend_rows(q_cpu_rows[:n], k_cpu, v_cpu, rows[:n], w.causal)
     dt = time.perf_counter() - t0
     fl = oracle.rows_flops(rows[:n], w.T, w.d, w.causal)
+    # the whole workload at the sample's rate, rows weighted by their key counts
+    full_s = useful_flops(w.B, w.H, w.T, w.d, w.causal) / (fl / dt)
     return {"value": fl / dt / 1e12, "unit": UNIT, "cores": n_thr, "kind": "oracle",
-            "sample": f"{n} sampled query rows of {w.name} (fp64 C, OpenMP over rows), {dt:.1f} s"}
+            "sample": f"{n} sampled query rows of {w.name} (fp64 C, OpenMP over rows), {dt:.1f} s",
+            "rows_per_s": n / dt, "fp64_gflops": fl / dt / 1e9, "full_workload_s_extrapolated": full_s}
 
 
 def run_reference(args, w):
@@ -213,6 +216,8 @@ def main():
     ap.add_argument("--no-fused", action="store_true", help="skip timing the fused-merge ring variant")
     ap.add_argument("--no-decode", action="store_true", help="skip timing decode on the million-token cache")
     ap.add_argument("--no-two-pass", action="store_true", help="skip timing the two-pass RSA form")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip timing the ring on the ragged and million-token workloads")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--shape", default=None,
                     help="B,H,T,d,N,causal: a bf16 normal-recipe workload instead of --workload (profiling)")
@@ -397,6 +402,38 @@ def main():
         del qt, kt, vt, ot, lt, wst, wsr
         torch.cuda.empty_cache()
 
+    # ---- the ring on the other synthetic workloads (median of 3 timed rings) --
+    others = None
+    if not args.no_other_workloads and world == 1:
+        others = {}
+        pk = read_peaks()
+        for name in ("ragged_causal_bf16", "million_causal_bf16"):
+            wo = rsa_inputs.WORKLOADS[name]
+            qo, ko, vo = rsa_inputs.make_workload(wo, seed=0, device=dev)
+            oo = torch.empty_like(qo)
+            lo = torch.empty((wo.B, wo.H, wo.T), dtype=torch.float32, device=dev)
+            wso = torch.empty(max(rsa.workspace_size(qo.dtype, wo.B, wo.H, wo.T, wo.d, wo.N, wo.causal), 1),
+                              dtype=torch.uint8, device=dev)
+            rsa.ring_attn(qo, ko, vo, wo.N, wo.causal, out=oo, lse=lo, workspace=wso)  # warm-up
+            torch.cuda.synchronize()
+            times = []
+            for _ in range(3):
+                a_ = torch.cuda.Event(enable_timing=True)
+                b_ = torch.cuda.Event(enable_timing=True)
+                a_.record(stream)
+                rsa.ring_attn(qo, ko, vo, wo.N, wo.causal, out=oo, lse=lo, workspace=wso)
+                b_.record(stream)
+                torch.cuda.synchronize()
+                times.append(a_.elapsed_time(b_))
+            rsa.check_device_error()
+            ms_o = sorted(times)[1]
+            tf_o = useful_flops(wo.B, wo.H, wo.T, wo.d, wo.causal) / (ms_o * 1e-3) / 1e12
+            others[name] = {"B": wo.B, "H": wo.H, "T": wo.T, "d": wo.d, "N": wo.N, "causal": wo.causal,
+                            "ms_per_ring_median_of_3": ms_o, "tflops": tf_o,
+                            "frac_of_sustained_bf16_peak": tf_o / pk["bf16_tflops_sustained"]}
+            del qo, ko, vo, oo, lo, wso
+            torch.cuda.empty_cache()
+
     # ---- end to end from pinned host memory (public API) --------------------
     e2e = None
     if args.e2e_steps > 0:
@@ -468,6 +505,7 @@ def main():
             "decode": dec,
             "two_pass_rsa": tp,
             "e2e": e2e,
+            "other_workloads": others,
             "gpu_launches": n_launch * args.steps,
             "cpu_baseline": cpu,
             "clocks": clk,
