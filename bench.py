@@ -136,6 +136,22 @@ def dist_info():
     return world, rank, local
 
 
+def max_over_ranks(pg, x: float, device) -> float:
+    """The largest x of all ranks (x itself when there is no process group):
+    a step of the whole job lasts as long as its slowest rank."""
+    if pg is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Throughput of the whole job: every rank's units over the slowest rank's time."""
+    return flops_per_rank * world / (ms_per_step * 1e-3) / 1e12
+
+
 def cpu_baseline(w, q_cpu_rows, k_cpu, v_cpu, rows, budget_s=15.0):
     """Time the oracle (as it stands) on a bounded sample of query rows."""
     import numpy as np
@@ -282,11 +298,7 @@ def main():
     barrier()
     clk = clocks.stop()
     rsa.check_device_error()
-    ms_total = t_start.elapsed_time(t_stop)
-    if pg is not None:
-        tt = torch.tensor([ms_total], device=dev)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(pg, t_start.elapsed_time(t_stop), dev)
     ms_step = ms_total / args.steps
 
     blk_ms = sum(ev0[s][i].elapsed_time(ev1[s][i]) for s in range(args.steps) for i in range(n_launch)
@@ -297,7 +309,7 @@ def main():
     n_mrg = sum(1 for x in kinds if x == 1)
 
     flops = useful_flops(B, H, T, d, causal)
-    value = flops * world / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(flops, world, ms_step)
     peaks = read_peaks()
     blk_tflops = flops / (blk_ms * 1e-3) / 1e12
     mbytes = merge_bytes_per_step(w, lambda r: rsa.ring_schedule(N, causal, r))
@@ -322,9 +334,9 @@ def main():
         torch.cuda.synchronize()
         barrier()
         rsa.check_device_error()
-        f_ms = t_start.elapsed_time(t_stop) / args.steps
+        f_ms = max_over_ranks(pg, t_start.elapsed_time(t_stop), dev) / args.steps
         f_blk = sum(fe0[s_][i].elapsed_time(fe1[s_][i]) for s_ in range(args.steps) for i in range(n_f)) / args.steps
-        f1 = {"value": flops * world / (f_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": f_ms,
+        f1 = {"value": whole_job_tflops(flops, world, f_ms), "unit": UNIT, "ms_per_step": f_ms,
               "block_kernel_tflops": flops / (f_blk * 1e-3) / 1e12, "launches_per_step": n_f,
               "workspace_bytes": int(ws_f.numel())}
         del ws_f
@@ -459,14 +471,10 @@ def main():
         e_clk = e_clocks.stop()
         barrier()
         e_steps = [e_ev[i].elapsed_time(e_ev[i + 1]) for i in range(args.e2e_steps)]
-        e_ms = sum(e_steps) / args.e2e_steps
-        if pg is not None:
-            tt = torch.tensor([e_ms], device=dev)
-            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-            e_ms = float(tt.item())
+        e_ms = max_over_ranks(pg, sum(e_steps) / args.e2e_steps, dev)
         h2d = 3 * qh.numel() * qh.element_size()
         d2h = bufs["out_host"].numel() * bufs["out_host"].element_size() + bufs["lse_host"].numel() * 4
-        e2e = {"value": flops * world / (e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
+        e2e = {"value": whole_job_tflops(flops, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "step_ms": [round(x, 2) for x in e_steps], "clocks": e_clk,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         k_cpu, v_cpu, q_cpu = kh, vh, qh
