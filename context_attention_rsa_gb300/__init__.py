@@ -288,28 +288,56 @@ def ring_launch_count(N: int, causal: bool, fused: bool = False) -> int:
     return n
 
 
+def slab_plan(BH: int, groups: int = 8, ramp: bool = True) -> List[int]:
+    """Heads per slab for ring_attn_from_host.
+
+    Without ramp: `groups` equal slabs.  With ramp: slabs of at most
+    ceil(BH / groups) heads in the middle, preceded by slabs that grow about
+    1.6x at a time from an eighth of that, and followed by slabs that shrink
+    back to an eighth.  Copying one head in takes less time than computing it,
+    so each slab's copy hides under its predecessor's ring.  What is left
+    exposed is the first slab's copy in and the last slab's copy out, and the
+    ramps keep those small."""
+    if BH <= 0:
+        return []
+    cap = max(1, -(-BH // max(1, min(int(groups), BH))))
+    if not ramp or cap < 8:
+        n = -(-BH // cap)
+        return [cap] * (BH // cap) + ([BH % cap] if BH % cap else []) if n > 0 else []
+    up, x = [], max(1, cap // 8)
+    while x < cap:
+        up.append(x)
+        x = max(x + 1, (x * 8) // 5)
+    down = [max(1, cap // 2), max(1, cap // 4), max(1, cap // 8)]
+    if sum(up) + sum(down) >= BH:
+        return slab_plan(BH, groups, ramp=False)
+    mid = BH - sum(up) - sum(down)
+    k = -(-mid // cap)  # middle slabs, as equal as possible
+    middle = [mid // k + (1 if i < mid % k else 0) for i in range(k)]
+    return up + middle + down
+
+
 def ring_attn_from_host(q_host, k_host, v_host, N: int, causal: bool, device=None, stream=None,
-                        buffers=None, groups: int = 8):
+                        buffers=None, groups: int = 8, ramp: bool = True):
     """End-to-end call from host memory: Q, K, V (host tensors, ideally pinned)
     in, out and lse (pinned host tensors) back.
 
-    Heads are independent problems, so the B*H heads are cut into ``groups``
-    contiguous slabs that stream through three CUDA streams: the copy of slab
-    g+1 to the device, the ring on slab g (C ABI, on ``stream`` or the current
-    stream) and the copy of slab g-1 back to the host all overlap.  Device
-    slabs are double-buffered.  The returned host tensors are complete once
-    ``stream`` has passed the call (it waits for the last copy back).
-    ``buffers`` (a dict, filled on first use) keeps the device slabs, the
-    workspace, the pinned outputs and the copy streams for reuse."""
+    Heads are independent problems, so the B*H heads are cut into slabs
+    (slab_plan(B*H, groups, ramp)) that stream through three CUDA streams: the
+    copy of slab g+1 to the device, the ring on slab g (C ABI, on ``stream``
+    or the current stream) and the copy of slab g-1 back to the host all
+    overlap.  Device slabs are double-buffered.  The returned host tensors are
+    complete once ``stream`` has passed the call (it waits for the last copy
+    back).  ``buffers`` (a dict, filled on first use) keeps the device slabs,
+    the workspace, the pinned outputs and the copy streams for reuse."""
     dev = torch.device(device) if device is not None else torch.device("cuda")
     b = buffers if buffers is not None else {}
     B, H, T, d = q_host.shape
     BH = B * H
-    G = max(1, min(int(groups), BH))
-    hg = (BH + G - 1) // G  # heads per slab
-    G = (BH + hg - 1) // hg
+    plan = slab_plan(BH, groups, ramp)
+    hg = max(plan)  # heads in the largest slab
     main = torch.cuda.current_stream(dev) if stream is None else stream
-    key = (tuple(q_host.shape), q_host.dtype, N, bool(causal), hg, str(dev))
+    key = (tuple(q_host.shape), q_host.dtype, N, bool(causal), tuple(plan), str(dev))
     if b.get("key") != key:
         b.clear()
         b["key"] = key
@@ -329,9 +357,9 @@ def ring_attn_from_host(q_host, k_host, v_host, N: int, causal: bool, device=Non
     s_in.wait_stream(main)
     s_out.wait_stream(main)
     ev_comp, ev_out = [], []
-    for g in range(G):
-        h0, h1 = g * hg, min(BH, (g + 1) * hg)
-        n = h1 - h0
+    h0 = 0
+    for g, n in enumerate(plan):
+        h1 = h0 + n
         slot = g % 2
         with torch.cuda.stream(s_in):
             if g >= 2:
@@ -356,6 +384,7 @@ def ring_attn_from_host(q_host, k_host, v_host, N: int, causal: bool, device=Non
             ev = torch.cuda.Event()
             ev.record(s_out)
             ev_out.append(ev)
+        h0 = h1
     main.wait_event(ev_out[-1])
     return b["out_host"], b["lse_host"], b
 

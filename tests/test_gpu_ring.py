@@ -196,16 +196,18 @@ def test_fused_and_unfused_rings_agree_and_fused_launches_only_block_kernels():
     assert torch.equal(out[:, :, :T // N], o_a[:, :, :T // N])  # chunk 0 is never merged
 
 
-@pytest.mark.parametrize("groups", [1, 3, 8])
-def test_ring_from_host_matches_device_ring(groups):
+@pytest.mark.parametrize("B,H,T,groups,ramp", [(2, 5, 1024, 1, True), (2, 5, 1024, 3, True), (2, 5, 1024, 8, True),
+                                                (1, 64, 512, 8, True), (1, 64, 512, 8, False)])
+def test_ring_from_host_matches_device_ring(B, H, T, groups, ramp):
     # The streamed host-to-host path (head slabs through three streams) gives
-    # exactly the device ring's result: every head is its own problem.
+    # exactly the device ring's result: every head is its own problem.  The
+    # 64-head cases run ramped slabs of 1 to 7 heads, and equal ones.
     need_cuda()
-    B, H, T, d, N = 2, 5, 1024, 128, 4
+    d, N = 128, 4
     q, k, v = (t.pin_memory() for t in qkv_cuda(B, H, T, d, torch.bfloat16, seed=13)[0])
     ref_o, ref_l = rsa.ring_attn(q.cuda(), k.cuda(), v.cuda(), N, True)
     bufs = {}
     for _ in range(2):  # second call reuses the buffers
-        oh, lh, bufs = rsa.ring_attn_from_host(q, k, v, N, True, buffers=bufs, groups=groups)
+        oh, lh, bufs = rsa.ring_attn_from_host(q, k, v, N, True, buffers=bufs, groups=groups, ramp=ramp)
         torch.cuda.synchronize()
         assert torch.equal(oh, ref_o.cpu()) and torch.equal(lh, ref_l.cpu())

@@ -172,3 +172,16 @@ def test_set_block_kernel_accepts_the_three_choices_only():
     assert lib.rsa_set_block_kernel(-1) == 1
     for which in (1, 2, 0):
         assert lib.rsa_set_block_kernel(which) == 0
+
+
+@pytest.mark.parametrize("BH,groups", [(512, 8), (512, 16), (64, 8), (100, 8), (37, 8), (7, 3), (1, 8), (512, 1)])
+def test_slab_plan_covers_every_head_and_ramps_gently(BH, groups):
+    plan = rsa.slab_plan(BH, groups)
+    assert sum(plan) == BH and all(n >= 1 for n in plan)
+    cap = -(-BH // min(groups, BH))
+    assert max(plan) <= cap
+    # each slab's copy-in must hide under its predecessor's ring: slabs grow by
+    # at most 1.6x (+1 for rounding) from one to the next
+    for a, b in zip(plan, plan[1:]):
+        assert b <= max(a + 1, (a * 8) // 5 + 1), plan
+    assert rsa.slab_plan(BH, groups, ramp=False) == [cap] * (BH // cap) + ([BH % cap] if BH % cap else [])
