@@ -136,6 +136,17 @@ def dist_info():
     return world, rank, local
 
 
+def two_pass_bytes(B, H, T, d, N, esz=2):
+    """HBM bytes one two-pass ring moves at the least.  Per query chunk: every
+    score is written (fp32) and read back by the row softmax, which writes P
+    (bf16) for the output pass to read: 12 bytes per score over the full
+    [Tc, T] rows.  Add Q and K read by the score pass, V by the output pass,
+    and out and lse written."""
+    BH, Tc = B * H, T // N
+    per_chunk = BH * Tc * T * (4 + 4 + 2 + 2) + BH * Tc * d * esz + 2 * BH * T * d * esz + BH * Tc * (d * esz + 4)
+    return per_chunk * N
+
+
 def max_over_ranks(pg, x: float, device) -> float:
     """The largest x of all ranks (x itself when there is no process group):
     a step of the whole job lasts as long as its slowest rank."""
@@ -411,6 +422,10 @@ def main():
               "workspace_bytes": int(wst.numel()), "online_ring_ms_per_step": timings["online_ring"],
               "online_ring_tflops": fl_t / (timings["online_ring"] * 1e-3) / 1e12,
               "online_ring_workspace_bytes": int(wsr.numel()), "launches_per_step": 3 * wt.N}
+        tb = two_pass_bytes(wt.B, wt.H, wt.T, wt.d, wt.N)
+        tp.update({"bound": "hbm", "algorithmic_bytes_per_step": tb,
+                   "achieved_gbs": tb / (timings["two_pass"] * 1e-3) / 1e9,
+                   "frac_of_measured_hbm": tb / (timings["two_pass"] * 1e-3) / 1e9 / read_peaks()["hbm_gbs"]})
         del qt, kt, vt, ot, lt, wst, wsr
         torch.cuda.empty_cache()
 
@@ -458,6 +473,17 @@ def main():
         _, _, bufs = rsa.ring_attn_from_host(qh, kh, vh, N, causal, device=dev)  # warm-up
         rsa.ring_attn_from_host(qh, kh, vh, N, causal, device=dev, buffers=bufs)
         torch.cuda.synchronize()
+        # host-to-device bandwidth just before the timed loop: one copy of Q's
+        # pinned host buffer (the link is shared with other work on the host)
+        probe = torch.empty_like(qh, device=dev)
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        probe.copy_(qh, non_blocking=True)
+        p1.record(stream)
+        torch.cuda.synchronize()
+        h2d_probe = qh.numel() * qh.element_size() / (p0.elapsed_time(p1) * 1e-3) / 1e9
+        del probe
         e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
         barrier()
         torch.cuda.synchronize()
@@ -476,6 +502,7 @@ def main():
         d2h = bufs["out_host"].numel() * bufs["out_host"].element_size() + bufs["lse_host"].numel() * 4
         e2e = {"value": whole_job_tflops(flops, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "step_ms": [round(x, 2) for x in e_steps], "clocks": e_clk,
+               "h2d_gbs_before": round(h2d_probe, 1),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         k_cpu, v_cpu, q_cpu = kh, vh, qh
     else:

@@ -451,7 +451,7 @@ rsa_status rsa_two_pass_workspace_size(rsa_dtype dt, int B, int H, int64_t T, in
         return fail(RSA_ERR_INVALID_ARG, "bytes is NULL");
     RSA_TRY(check_two_pass(dt, B, H, T, d, N));
     const size_t rows = (size_t)B * H * (size_t)(T / N);
-    *bytes = align256(rows * (size_t)T * 4) + align256(rows * (size_t)T * 2);
+    *bytes = align256(rows * (size_t)T * 4) + align256(rows * (size_t)T * 2) + align256(rows * (size_t)(T / 128) * 8);
     return RSA_OK;
 }
 
@@ -476,8 +476,9 @@ rsa_status rsa_two_pass_attn_fwd(const void *q, const void *k, const void *v, rs
     const size_t rows = (size_t)B * H * (size_t)(T / N);
     float *S = static_cast<float *>(workspace);
     void *P = static_cast<char *>(workspace) + align256(rows * (size_t)T * 4);
-    cudaError_t e = launch_two_pass(q, k, v, (int64_t)B * H, T, N, causal, out, lse, S, P, g_wait_limit_ns.load(),
-                                    err, stream);
+    void *stats = static_cast<char *>(P) + align256(rows * (size_t)T * 2);
+    cudaError_t e = launch_two_pass(q, k, v, (int64_t)B * H, T, N, causal, out, lse, S, P, stats,
+                                    g_wait_limit_ns.load(), err, stream);
     if (e != cudaSuccess)
         return fail(RSA_ERR_CUDA, "two-pass launch: %s", cudaGetErrorString(e));
     return RSA_OK;

@@ -93,16 +93,20 @@ cudaError_t launch_merge_splits(const float *o_part, const float *lse_part, int 
                                 void *out, int out_f32, float *lse, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint64_t limit_ns, unsigned int *err, cudaStream_t s);
 // Two-pass ring self-attention (bf16, d = 128, T/N a multiple of 128): per
-// query chunk, score pass into S [BH, Tc, T] fp32, row softmax into P
-// [BH, Tc, T] bf16 (and lse), output pass into out.
+// query chunk, score pass into S [BH, Tc, T] fp32 (and per-tile row
+// statistics [BH, Tc, T/128] float2), row softmax into P [BH, Tc, T] bf16
+// (and lse), output pass into out.
 cudaError_t launch_two_pass(const void *q, const void *k, const void *v, int64_t BH, int64_t T, int N, int causal,
-                            void *out, float *lse, float *S, void *P, uint64_t wait_limit_ns, unsigned int *err,
-                            cudaStream_t s);
+                            void *out, float *lse, float *S, void *P, void *stats, uint64_t wait_limit_ns,
+                            unsigned int *err, cudaStream_t s);
 
 // bf16 TMA tensor map with 128-byte swizzle: dims and box innermost first,
 // strides in bytes for dimensions 1..rank-1.  False if the driver rejects it.
 bool make_bf16_map_sw128(CUtensorMap *m, const void *ptr, int rank, const uint64_t *dims,
                          const uint64_t *strides_bytes, const uint32_t *box);
+// The same for fp32 elements.
+bool make_f32_map_sw128(CUtensorMap *m, const void *ptr, int rank, const uint64_t *dims,
+                        const uint64_t *strides_bytes, const uint32_t *box);
 
 // Rows of one CTA of the tensor-core kernel (two 128-row tiles).
 constexpr int kBf16RowsPerCta = 256;

@@ -28,8 +28,10 @@ EncodeTiledFn encode_fn()
 
 }  // namespace
 
-bool make_bf16_map_sw128(CUtensorMap *m, const void *ptr, int rank, const uint64_t *dims,
-                         const uint64_t *strides_bytes, const uint32_t *box)
+namespace {
+
+bool make_map_sw128(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, int rank, const uint64_t *dims,
+                    const uint64_t *strides_bytes, const uint32_t *box)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn || rank < 1 || rank > 5)
@@ -44,10 +46,23 @@ bool make_bf16_map_sw128(CUtensorMap *m, const void *ptr, int rank, const uint64
         if (i + 1 < rank)
             st[i] = strides_bytes[i];
     }
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(ptr), d, st, bx, es,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void *>(ptr), d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool make_bf16_map_sw128(CUtensorMap *m, const void *ptr, int rank, const uint64_t *dims,
+                         const uint64_t *strides_bytes, const uint32_t *box)
+{
+    return make_map_sw128(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, rank, dims, strides_bytes, box);
+}
+
+bool make_f32_map_sw128(CUtensorMap *m, const void *ptr, int rank, const uint64_t *dims,
+                        const uint64_t *strides_bytes, const uint32_t *box)
+{
+    return make_map_sw128(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ptr, rank, dims, strides_bytes, box);
 }
 
 }  // namespace rsa

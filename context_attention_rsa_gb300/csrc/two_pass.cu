@@ -11,8 +11,11 @@
 // buffer -- the O(L/N * L) memory the online merge avoids.  Chunks are done one
 // after another, reusing the buffers:
 //   score kernel   S^n = Q_n K^T / sqrt(d) (tcgen05, one 128x128 tile per CTA),
-//                  causal entries set to -inf
-//   softmax kernel row max and sum over the whole row (one warp per row),
+//                  causal entries set to -inf.  The tile is staged in shared
+//                  memory and written by TMA stores; each row also leaves the
+//                  tile's (max, sum of e^{s - max}) in a small statistics buffer
+//   softmax kernel row max and sum over the whole row from those statistics
+//                  (one warp per row), then one pass over the row:
 //                  P^n = e^{s - m} / l in bf16, lse = m + ln l
 //   PV kernel      O^n = sum over key chunks in ring order (n - r) mod N of
 //                  P^n_j V_j (tcgen05, 128 rows per CTA, fp32 accumulator)
@@ -37,6 +40,7 @@ struct TwoPassParams {
     int N;
     int causal;
     float *S;              // [BH, Tc, T] fp32 scores of chunk n
+    float2 *stats;         // [BH, Tc, T/128]: per row and key tile, (max, sum of e^{s - max})
     __nv_bfloat16 *out;    // [BH, T, d]
     uint64_t wait_limit_ns;
     unsigned int *err;
@@ -44,10 +48,38 @@ struct TwoPassParams {
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d)
+{
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+// Named barrier 1 over the 128 epilogue threads (warps 0-3); the reducing
+// form returns whether `v` holds in all of them.
+__device__ __forceinline__ void epi_bar_sync()
+{
+    asm volatile("barrier.cta.sync 1, 128;" ::: "memory");
+}
+
+__device__ __forceinline__ bool epi_bar_and(bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "barrier.cta.red.and.pred po, 1, 128, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
 // S^n tile (qt, kt): 128 query rows of chunk n against keys kt*128 .. +127.
 __global__ void __launch_bounds__(kThreads)
     score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ TwoPassParams p)
+                 const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ TwoPassParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -109,11 +141,15 @@ __global__ void __launch_bounds__(kThreads)
             ok = ptx::mbar_wait(bar_mma, 0, p.wait_limit_ns, abort_flag, p.err, 43);
             ok = __all_sync(0xffffffffu, ok);
         }
+        ok = epi_bar_and(ok);  // all four warps go on, or none
         if (ok) {
+            // The MMA has finished reading Q and K, so their 64 KB hold the fp32
+            // tile for the TMA store: four boxes of 32 columns x 128 rows, each
+            // 128-byte row with its 16-byte pieces swizzled by the row (the
+            // map's 128-byte swizzle).
             ptx::tc_fence_after();
             const float scale = 1.0f / sqrtf((float)D);
-            const bool valid = (int64_t)qt * 128 + row < p.Tc;
-            float *dst = p.S + ((int64_t)bh * p.Tc + (int64_t)qt * 128 + row) * p.T + k0;
+            float rm = -INFINITY, rl = 0.f;  // this row's max and sum of e^{s - max} over the tile
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t s[32];
@@ -121,20 +157,40 @@ __global__ void __launch_bounds__(kThreads)
                     ptx::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c * 32, s);
                     ptx::tmem_ld_wait(s);
                 }
-                if (valid) {
-                    float v[32];
+                float v[32];
+                float cm = -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int64_t key = k0 + c * 32 + i;
-                        const bool masked = all_masked || (p.causal && key > qpos);
-                        v[i] = masked ? -INFINITY : u2f(s[i]) * scale;
-                    }
-                    float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                for (int i = 0; i < 32; ++i) {
+                    const int64_t key = k0 + c * 32 + i;
+                    const bool masked = all_masked || (p.causal && key > qpos);
+                    v[i] = masked ? -INFINITY : u2f(s[i]) * scale;
+                    cm = fmaxf(cm, v[i]);
                 }
+                const float nm = fmaxf(rm, cm);
+                if (nm > -INFINITY) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        acc += ptx::ex2((v[i] - nm) * kLog2e);
+                    rl = rl * ptx::ex2((rm - nm) * kLog2e) + acc;
+                    rm = nm;
+                }
+                const uint32_t line = base + (uint32_t)c * kBoxBytes + (uint32_t)row * 128u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(line + ((uint32_t)(j ^ (row & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                                 v[4 * j + 3]);
             }
+            ptx::fence_proxy_async_smem();
+            epi_bar_sync();
+            if (threadIdx.x == 0) {
+                for (int c = 0; c < 4; ++c)
+                    ptx::tma_store_3d(&tm_s, base + (uint32_t)c * kBoxBytes, (int)(k0 + c * 32), qt * 128, (int)bh);
+                ptx::bulk_commit_group();
+                ptx::bulk_wait_group_read0();  // shared memory stays in use until the stores have read it
+            }
+            if ((int64_t)qt * 128 + row < p.Tc)
+                p.stats[((int64_t)bh * p.Tc + (int64_t)qt * 128 + row) * (p.T / 128) + kt] = make_float2(rm, rl);
         }
     }
     ptx::tc_fence_before();
@@ -145,55 +201,56 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-// Softmax over each full score row of chunk n (one warp per row): P = e^{s-m}/l
-// in bf16, lse = m + ln l into the output lse.
+// Softmax over each full score row of chunk n (one warp per row): the row's
+// max M and sum L from the per-tile statistics, then one pass over the row,
+// P = e^{s-M}/L in bf16, and lse = M + ln L into the output lse.
 __global__ void __launch_bounds__(256)
-    softmax_rows_kernel(const float *__restrict__ S, __nv_bfloat16 *__restrict__ P, float *__restrict__ lse,
-                        int64_t BH, int64_t Tc, int64_t T, int n)
+    softmax_rows_kernel(const float *__restrict__ S, const float2 *__restrict__ stats, __nv_bfloat16 *__restrict__ P,
+                        float *__restrict__ lse, int64_t BH, int64_t Tc, int64_t T, int n)
 {
     const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= BH * Tc)
         return;
-    const float4 *src = reinterpret_cast<const float4 *>(S + row * T);
-    const int64_t n4 = T / 4;
-    // online max and sum over the lane's elements
-    float m = -INFINITY, l = 0.f;
-    for (int64_t i = lane; i < n4; i += 32) {
-        const float4 x = src[i];
-        const float mx = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
-        const float mn = fmaxf(m, mx);
-        if (mn > -INFINITY) {
-            l = l * expf(m - mn) + expf(x.x - mn) + expf(x.y - mn) + expf(x.z - mn) + expf(x.w - mn);
-            m = mn;
-        }
-    }
-    float M = m;
+    const int64_t n_kt = T / 128;
+    const float2 *st = stats + row * n_kt;
+    float M = -INFINITY;
+    for (int64_t i = lane; i < n_kt; i += 32)
+        M = fmaxf(M, st[i].x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float lw = (m > -INFINITY) ? l * expf(m - M) : 0.f;
+    float L = 0.f;
+    if (M > -INFINITY) {
+        for (int64_t i = lane; i < n_kt; i += 32) {
+            const float2 x = st[i];
+            if (x.x > -INFINITY)
+                L += x.y * ptx::ex2((x.x - M) * kLog2e);
+        }
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
-        lw += __shfl_xor_sync(0xffffffffu, lw, o);
-    const bool empty = !(lw > 0.f);
-    const float inv = empty ? 0.f : 1.f / lw;
+        L += __shfl_xor_sync(0xffffffffu, L, o);
+    const bool empty = !(L > 0.f);
+    const float inv = empty ? 0.f : 1.f / L;
+    const float mM = empty ? 0.f : M * kLog2e;
+    const float4 *src = reinterpret_cast<const float4 *>(S + row * T);
     uint2 *dst = reinterpret_cast<uint2 *>(P + row * T);
-    for (int64_t i = lane; i < n4; i += 32) {
+    for (int64_t i = lane; i < T / 4; i += 32) {
         const float4 x = src[i];
         float e[4] = {0.f, 0.f, 0.f, 0.f};
         if (!empty) {
-            e[0] = expf(x.x - M) * inv;
-            e[1] = expf(x.y - M) * inv;
-            e[2] = expf(x.z - M) * inv;
-            e[3] = expf(x.w - M) * inv;
+            e[0] = ptx::ex2(fmaf(x.x, kLog2e, -mM)) * inv;
+            e[1] = ptx::ex2(fmaf(x.y, kLog2e, -mM)) * inv;
+            e[2] = ptx::ex2(fmaf(x.z, kLog2e, -mM)) * inv;
+            e[3] = ptx::ex2(fmaf(x.w, kLog2e, -mM)) * inv;
         }
         __nv_bfloat162 a = __floats2bfloat162_rn(e[0], e[1]), b = __floats2bfloat162_rn(e[2], e[3]);
         dst[i] = make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
     }
     if (lane == 0) {
         const int64_t bh = row / Tc, r = row - bh * Tc;
-        lse[bh * T + (int64_t)n * Tc + r] = empty ? -INFINITY : M + logf(lw);
+        lse[bh * T + (int64_t)n * Tc + r] = empty ? -INFINITY : M + ptx::lg2(L) * 0.69314718055994531f;
     }
 }
 
@@ -338,11 +395,11 @@ __global__ void __launch_bounds__(kThreads)
 }  // namespace
 
 cudaError_t launch_two_pass(const void *q, const void *k, const void *v, int64_t BH, int64_t T, int N, int causal,
-                            void *out, float *lse, float *S, void *P, uint64_t wait_limit_ns, unsigned int *err,
-                            cudaStream_t s)
+                            void *out, float *lse, float *S, void *P, void *stats, uint64_t wait_limit_ns,
+                            unsigned int *err, cudaStream_t s)
 {
     const int64_t Tc = T / N;
-    CUtensorMap mq, mk, mv, mp;
+    CUtensorMap mq, mk, mv, mp, ms;
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)T, (uint64_t)BH};
     const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)T * D * 2};
     const uint32_t box[3] = {64, 128, 1};
@@ -350,6 +407,11 @@ cudaError_t launch_two_pass(const void *q, const void *k, const void *v, int64_t
     const uint64_t pstrides[2] = {(uint64_t)T * 2, (uint64_t)Tc * T * 2};
     if (!make_bf16_map_sw128(&mq, q, 3, dims, strides, box) || !make_bf16_map_sw128(&mk, k, 3, dims, strides, box) ||
         !make_bf16_map_sw128(&mv, v, 3, dims, strides, box) || !make_bf16_map_sw128(&mp, P, 3, pdims, pstrides, box))
+        return cudaErrorInvalidValue;
+    // S [BH][Tc][T] fp32, written in 32-column x 128-row boxes (128 bytes wide)
+    const uint64_t sstrides[2] = {(uint64_t)T * 4, (uint64_t)Tc * T * 4};
+    const uint32_t sbox[3] = {32, 128, 1};
+    if (!make_f32_map_sw128(&ms, S, 3, pdims, sstrides, sbox))
         return cudaErrorInvalidValue;
     const uint32_t smem_score = 2 * kTileBytes + 64 + 1024, smem_pv = 4 * kTileBytes + 64 + 1024;
     cudaError_t e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_score);
@@ -369,13 +431,14 @@ cudaError_t launch_two_pass(const void *q, const void *k, const void *v, int64_t
         p.N = N;
         p.causal = causal ? 1 : 0;
         p.S = S;
+        p.stats = static_cast<float2 *>(stats);
         p.out = static_cast<__nv_bfloat16 *>(out);
         p.wait_limit_ns = wait_limit_ns;
         p.err = err;
-        score_kernel<<<dim3((unsigned)n_qt, (unsigned)n_kt, (unsigned)BH), kThreads, smem_score, s>>>(mq, mk, p);
+        score_kernel<<<dim3((unsigned)n_qt, (unsigned)n_kt, (unsigned)BH), kThreads, smem_score, s>>>(mq, mk, ms, p);
         const int64_t rows = BH * Tc;
-        softmax_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(S, static_cast<__nv_bfloat16 *>(P), lse, BH,
-                                                                       Tc, T, n);
+        softmax_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
+            S, static_cast<const float2 *>(stats), static_cast<__nv_bfloat16 *>(P), lse, BH, Tc, T, n);
         pv_kernel<<<dim3((unsigned)n_qt, (unsigned)BH), kThreads, smem_pv, s>>>(mp, mv, p);
         e = cudaGetLastError();
         if (e != cudaSuccess)
