@@ -464,9 +464,9 @@ def main():
     # ---- end to end from pinned host memory (public API) --------------------
     e2e = None
     if args.e2e_steps > 0:
-        qh = q.cpu().pin_memory()
-        kh = k.cpu().pin_memory()
-        vh = v.cpu().pin_memory()
+        qh, kh, vh = (rsa.host_empty(t.shape, t.dtype) for t in (q, k, v))
+        for th, td in ((qh, q), (kh, k), (vh, v)):
+            th.copy_(td)
         del q, k, v, out, lse, ws
         torch.cuda.empty_cache()
         bufs = None

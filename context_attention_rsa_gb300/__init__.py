@@ -14,7 +14,9 @@ softmax seems to require all attention scores at once") and causal skipping
 """
 from __future__ import annotations
 
+import atexit
 import ctypes
+import mmap
 import threading
 from typing import List, Optional, Sequence, Tuple
 
@@ -25,7 +27,8 @@ from . import _build
 __all__ = [
     "RsaError", "load", "library_path", "block_attn_fwd", "merge", "merge_finalize",
     "ring_attn", "ring_attn_noalloc", "ring_attn_timed", "decode_attn", "decode_workspace_size",
-    "two_pass_attn", "two_pass_workspace_size", "ring_attn_from_host", "workspace_size", "ring_schedule",
+    "two_pass_attn", "two_pass_workspace_size", "ring_attn_from_host", "slab_plan", "host_empty", "host_free",
+    "workspace_size", "ring_schedule", "set_block_kernel",
     "set_wait_limit_ns", "check_device_error", "selftest_wait_timeout", "version",
     "RSA_F32", "RSA_BF16",
 ]
@@ -288,6 +291,92 @@ def ring_launch_count(N: int, causal: bool, fused: bool = False) -> int:
     return n
 
 
+# Page-locked host blocks made by host_empty: storage address -> (mmap, bytes, base tensor).
+_host_blocks = {}
+_host_lock = threading.Lock()
+
+
+def _huge_bytes(addr: int) -> int:
+    """Bytes of the mapping that contains addr that sit on transparent huge
+    pages (AnonHugePages in /proc/self/smaps); 0 if it cannot be read."""
+    try:
+        with open("/proc/self/smaps") as f:
+            inside = False
+            for line in f:
+                head = line.split(None, 1)[0]
+                if "-" in head and ":" not in head:
+                    lo, hi = (int(x, 16) for x in head.split("-"))
+                    inside = lo <= addr < hi
+                elif inside and head == "AnonHugePages:":
+                    return int(line.split()[1]) * 1024
+    except (OSError, ValueError):
+        pass
+    return 0
+
+
+def host_empty(shape, dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
+    """A page-locked host tensor for streaming copies, on transparent huge
+    pages where the host can provide them.
+
+    The memory is an anonymous mapping advised for huge pages and touched, so
+    that its pages exist.  If at least 90% of it landed on huge pages it is
+    registered with cudaHostRegister.  Copies from and to such a block keep
+    their rate when the host's memory is fragmented: with scattered small
+    pinned pages, concurrent copies in and out have been measured to slow
+    down by up to 2x in some steps.  Otherwise (small pages only, where a
+    registered block copies several times slower than a driver-pinned one)
+    the tensor comes from torch's pinned allocator instead.
+
+    A registered block stays registered until host_free() is called on the
+    tensor (or a view of its storage), or the process exits."""
+    shape = tuple(int(x) for x in shape)
+    numel = 1
+    for x in shape:
+        numel *= x
+    nbytes = numel * torch.empty((), dtype=dtype).element_size()
+    size = max(1, (nbytes + (2 << 20) - 1) // (2 << 20)) * (2 << 20)
+    if hasattr(mmap, "MADV_HUGEPAGE"):
+        m = mmap.mmap(-1, size, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS, prot=mmap.PROT_READ | mmap.PROT_WRITE)
+        m.madvise(mmap.MADV_HUGEPAGE)
+        raw = torch.frombuffer(m, dtype=torch.uint8, count=size)
+        raw.fill_(0)
+        if _huge_bytes(raw.data_ptr()) >= 0.9 * size:
+            err = torch.cuda.cudart().cudaHostRegister(raw.data_ptr(), size, 0)
+            if int(err) != 0:
+                raise RsaError("host_empty", 3, f"cudaHostRegister of {size} bytes failed: {err}")
+            with _host_lock:
+                _host_blocks[raw.data_ptr()] = (m, size, raw)
+            return raw[:nbytes].view(dtype).view(shape)
+        del raw
+        try:
+            m.close()
+        except BufferError:
+            pass  # closed when the last reference goes
+    return torch.empty(shape, dtype=dtype, pin_memory=True)
+
+
+def host_free(t: torch.Tensor) -> None:
+    """Unregister a block made by host_empty (the memory itself goes away with
+    its last tensor).  Tensors not made by host_empty are left alone."""
+    ptr = t.untyped_storage().data_ptr()
+    with _host_lock:
+        blk = _host_blocks.pop(ptr, None)
+    if blk is not None:
+        torch.cuda.cudart().cudaHostUnregister(ptr)
+
+
+@atexit.register
+def _host_free_all():
+    with _host_lock:
+        ptrs = list(_host_blocks)
+        _host_blocks.clear()
+    for ptr in ptrs:
+        try:
+            torch.cuda.cudart().cudaHostUnregister(ptr)
+        except Exception:
+            pass
+
+
 def slab_plan(BH: int, groups: int = 8, ramp: bool = True) -> List[int]:
     """Heads per slab for ring_attn_from_host.
 
@@ -319,8 +408,8 @@ def slab_plan(BH: int, groups: int = 8, ramp: bool = True) -> List[int]:
 
 def ring_attn_from_host(q_host, k_host, v_host, N: int, causal: bool, device=None, stream=None,
                         buffers=None, groups: int = 8, ramp: bool = True):
-    """End-to-end call from host memory: Q, K, V (host tensors, ideally pinned)
-    in, out and lse (pinned host tensors) back.
+    """End-to-end call from host memory: Q, K, V (host tensors, ideally made
+    by host_empty) in, out and lse (page-locked host tensors) back.
 
     Heads are independent problems, so the B*H heads are cut into slabs
     (slab_plan(B*H, groups, ramp)) that stream through three CUDA streams: the
@@ -339,6 +428,9 @@ def ring_attn_from_host(q_host, k_host, v_host, N: int, causal: bool, device=Non
     main = torch.cuda.current_stream(dev) if stream is None else stream
     key = (tuple(q_host.shape), q_host.dtype, N, bool(causal), tuple(plan), str(dev))
     if b.get("key") != key:
+        for name in ("out_host", "lse_host"):
+            if name in b:
+                host_free(b[name])
         b.clear()
         b["key"] = key
         mk = lambda *shape, dt=q_host.dtype: torch.empty(shape, dtype=dt, device=dev)
@@ -346,8 +438,8 @@ def ring_attn_from_host(q_host, k_host, v_host, N: int, causal: bool, device=Non
         b["out"] = [mk(hg, T, d) for _ in range(2)]
         b["lse"] = [mk(hg, T, dt=torch.float32) for _ in range(2)]
         b["ws"] = mk(max(workspace_size(q_host.dtype, 1, hg, T, d, N, causal), 1), dt=torch.uint8)
-        b["out_host"] = torch.empty(q_host.shape, dtype=q_host.dtype, pin_memory=True)
-        b["lse_host"] = torch.empty((B, H, T), dtype=torch.float32, pin_memory=True)
+        b["out_host"] = host_empty(q_host.shape, q_host.dtype)
+        b["lse_host"] = host_empty((B, H, T), torch.float32)
         b["s_in"] = torch.cuda.Stream(dev)
         b["s_out"] = torch.cuda.Stream(dev)
     s_in, s_out = b["s_in"], b["s_out"]

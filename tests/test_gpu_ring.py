@@ -211,3 +211,26 @@ def test_ring_from_host_matches_device_ring(B, H, T, groups, ramp):
         oh, lh, bufs = rsa.ring_attn_from_host(q, k, v, N, True, buffers=bufs, groups=groups, ramp=ramp)
         torch.cuda.synchronize()
         assert torch.equal(oh, ref_o.cpu()) and torch.equal(lh, ref_l.cpu())
+
+
+def test_host_empty_is_page_locked_and_streams_bit_exactly():
+    need_cuda()
+    B, H, T, d, N = 1, 64, 512, 128, 4
+    (q, k, v), _ = qkv_cuda(B, H, T, d, torch.bfloat16, seed=21)
+    qh, kh, vh = (rsa.host_empty(t.shape, t.dtype) for t in (q, k, v))
+    for th, t in ((qh, q), (kh, k), (vh, v)):
+        th.copy_(t)
+        assert th.is_pinned() and torch.equal(th, t)
+    ref_o, ref_l = rsa.ring_attn(q.cuda(), k.cuda(), v.cuda(), N, True)
+    bufs = {}
+    oh, lh, bufs = rsa.ring_attn_from_host(qh, kh, vh, N, True, buffers=bufs)
+    torch.cuda.synchronize()
+    assert bufs["out_host"].is_pinned() and bufs["lse_host"].is_pinned()
+    assert torch.equal(oh, ref_o.cpu()) and torch.equal(lh, ref_l.cpu())
+    for th in (qh, kh, vh):
+        # a block on huge pages is registered by host_empty and unregistered by
+        # host_free; otherwise it came from torch's pinned allocator
+        registered = th.untyped_storage().data_ptr() in rsa._host_blocks
+        rsa.host_free(th)
+        assert th.is_pinned() != registered
+    rsa.host_free(q)  # not made by host_empty: left alone
