@@ -135,25 +135,59 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-// Fold S partial results of the same rows (split-KV decode): one warp per row.
+// Fold S partial results of the same rows (split-KV decode): one CTA per row.
 // M = max_s lse_s, L = M + ln sum_s e^{lse_s - M}, o = sum_s o_s e^{lse_s - L};
-// rows whose partials are all empty stay (0, -inf).
+// rows whose partials are all empty stay (0, -inf).  The eight warps share
+// the splits (warp w takes s = w, w + 8, ...), so their loads are in flight
+// together, and add their partial sums through shared memory.
+constexpr int kSplitWarps = 8;
+
+__device__ __forceinline__ float block_max(float v, float *red)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int w = 1; w < kSplitWarps; ++w)
+        r = fmaxf(r, red[w]);
+    return r;
+}
+
+__device__ __forceinline__ float block_sum(float v, float *red)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSplitWarps; ++w)
+        r += red[w];
+    return r;
+}
+
 template <int PER>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(32 * kSplitWarps)
     merge_splits_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part, int S, int64_t rows,
                         void *out, int out_f32, float *lse)
 {
     constexpr int D = PER * 32;
-    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= rows)
-        return;
-    float M = -INFINITY;
-    for (int s = lane; s < S; s += 32)
-        M = fmaxf(M, lse_part[(int64_t)s * rows + row]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    __shared__ float red[kSplitWarps];
+    __shared__ float part[kSplitWarps][D];
+    const int64_t row = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float m = -INFINITY;
+    for (int s = threadIdx.x; s < S; s += 32 * kSplitWarps)
+        m = fmaxf(m, lse_part[(int64_t)s * rows + row]);
+    const float M = block_max(m, red);
     float acc[PER];
 #pragma unroll
     for (int c = 0; c < PER; ++c)
@@ -161,21 +195,32 @@ __global__ void __launch_bounds__(256)
     float L = -INFINITY;
     if (M > -INFINITY) {
         float sum = 0.f;
-        for (int s = lane; s < S; s += 32)
+        for (int s = threadIdx.x; s < S; s += 32 * kSplitWarps)
             sum += expf(lse_part[(int64_t)s * rows + row] - M);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        L = M + logf(sum);
-        for (int s = 0; s < S; ++s) {
+        L = M + logf(block_sum(sum, red));
+        // an empty split has lse = -inf (weight 0) and o = 0
+#pragma unroll 4
+        for (int s = warp; s < S; s += kSplitWarps) {
             const float w = expf(lse_part[(int64_t)s * rows + row] - L);
-            if (w == 0.f)
-                continue;
             const float *src = o_part + ((int64_t)s * rows + row) * D + lane * PER;
 #pragma unroll
             for (int c = 0; c < PER; ++c)
                 acc[c] = fmaf(w, src[c], acc[c]);
         }
+    }
+#pragma unroll
+    for (int c = 0; c < PER; ++c)
+        part[warp][lane * PER + c] = acc[c];
+    __syncthreads();
+    if (warp != 0)
+        return;
+#pragma unroll
+    for (int c = 0; c < PER; ++c) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kSplitWarps; ++w)
+            v += part[w][lane * PER + c];
+        acc[c] = v;
     }
     if (out_f32) {
         float *dst = static_cast<float *>(out) + row * D + lane * PER;
@@ -199,13 +244,12 @@ cudaError_t launch_merge_splits(const float *o_part, const float *lse_part, int 
 {
     if (rows <= 0 || S <= 0)
         return cudaSuccess;
-    const int64_t blocks = (rows + 7) / 8;
-    if (blocks > 0x7fffffffLL)
+    if (rows > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     if (d == 128)
-        merge_splits_kernel<4><<<(unsigned)blocks, 256, 0, s>>>(o_part, lse_part, S, rows, out, out_f32, lse);
+        merge_splits_kernel<4><<<(unsigned)rows, 32 * kSplitWarps, 0, s>>>(o_part, lse_part, S, rows, out, out_f32, lse);
     else if (d == 64)
-        merge_splits_kernel<2><<<(unsigned)blocks, 256, 0, s>>>(o_part, lse_part, S, rows, out, out_f32, lse);
+        merge_splits_kernel<2><<<(unsigned)rows, 32 * kSplitWarps, 0, s>>>(o_part, lse_part, S, rows, out, out_f32, lse);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();
