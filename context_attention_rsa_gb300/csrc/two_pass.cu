@@ -255,7 +255,9 @@ __global__ void __launch_bounds__(256)
 }
 
 // O^n rows qt*128.. of head bh: sum over key chunks j in ring order (n - r) mod N
-// of P^n_j V_j, 128 keys per step, two shared-memory stages.
+// of P^n_j V_j, 128 keys per step, kPvStages shared-memory stages.
+constexpr int kPvStages = 3;
+
 __global__ void __launch_bounds__(kThreads)
     pv_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_v,
               const __grid_constant__ TwoPassParams p)
@@ -265,9 +267,9 @@ __global__ void __launch_bounds__(kThreads)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *g = smem_raw + (base - raw);
     // stage s: P tile at base + s*2*kTileBytes, V tile right after it
-    const uint32_t bars = base + 4 * kTileBytes;  // full[2], empty[2], done
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(g + 4 * kTileBytes + 48);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(g + 4 * kTileBytes + 52);
+    const uint32_t bars = base + 2 * kPvStages * kTileBytes;  // full[kPvStages], empty[kPvStages], done
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(g + 2 * kPvStages * kTileBytes + 16 * kPvStages + 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(g + 2 * kPvStages * kTileBytes + 16 * kPvStages + 20);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qt = blockIdx.x, bh = blockIdx.y;
     const int64_t tiles_per_chunk = p.Tc / 128;
@@ -275,7 +277,7 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t nt = tiles_per_chunk * chunks;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 5; ++i)
+        for (int i = 0; i < 2 * kPvStages + 1; ++i)
             ptx::mbar_init(bars + 8 * i, 1);
         *abort_flag = 0;
         ptx::fence_barrier_init();
@@ -289,8 +291,8 @@ __global__ void __launch_bounds__(kThreads)
     ptx::tc_fence_after();
     const uint32_t tmem = *tslot;
     auto FULL = [&](int s) { return bars + 8u * s; };
-    auto EMPTY = [&](int s) { return bars + 16u + 8u * s; };
-    const uint32_t DONE = bars + 32u;
+    auto EMPTY = [&](int s) { return bars + 8u * kPvStages + 8u * s; };
+    const uint32_t DONE = bars + 16u * kPvStages;
 
     if (warp == 4) {
         if (lane == 0) {
@@ -301,7 +303,7 @@ __global__ void __launch_bounds__(kThreads)
                 return j * p.Tc + (i - r * tiles_per_chunk) * 128;
             };
             auto load = [&](int64_t i) {
-                const int s = (int)(i & 1);
+                const int s = (int)(i % kPvStages);
                 const uint32_t sp = base + s * 2 * kTileBytes, sv = sp + kTileBytes;
                 const int64_t kk0 = key0(i);
                 ptx::mbar_arrive_expect_tx(FULL(s), 2 * kTileBytes);
@@ -315,22 +317,15 @@ __global__ void __launch_bounds__(kThreads)
             const uint64_t dv0 = ptx::smem_desc_sw128(base + kTileBytes, kBoxBytes, 1024);
             bool ok = true;
             int64_t issued = 0;
-            if (nt > 0) {
-                load(0);
-                issued = 1;
-            }
+            // tile i uses stage i % kPvStages; its fill is that stage's (i / kPvStages)-th.
+            // Each step issues tile i's MMAs first and only then waits for tile
+            // i-1's to free their stage for tile i + kPvStages - 1, so the
+            // tensor core always has the next tile queued.
+            for (; issued < nt && issued < kPvStages - 1; ++issued)
+                load(issued);
             for (int64_t i = 0; ok && i < nt; ++i) {
-                if (i + 1 < nt) {
-                    if (i + 1 >= 2)
-                        ok = ptx::mbar_wait(EMPTY((int)((i + 1) & 1)), (uint32_t)(((i + 1) / 2 - 1) & 1),
-                                            p.wait_limit_ns, abort_flag, p.err, 50);
-                    if (!ok)
-                        break;
-                    load(i + 1);
-                    issued = i + 2;
-                }
-                const int s = (int)(i & 1);
-                ok = ptx::mbar_wait(FULL(s), (uint32_t)((i / 2) & 1), p.wait_limit_ns, abort_flag, p.err, 51);
+                const int s = (int)(i % kPvStages);
+                ok = ptx::mbar_wait(FULL(s), (uint32_t)((i / kPvStages) & 1), p.wait_limit_ns, abort_flag, p.err, 51);
                 if (!ok)
                     break;
                 const uint64_t pa = dp0 + ((s * 2 * kTileBytes) >> 4);
@@ -341,13 +336,24 @@ __global__ void __launch_bounds__(kThreads)
                     ptx::mma_ss(tmem, pa + off, vb + ((kk * 2048) >> 4), idesc, (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 ptx::mma_commit(EMPTY(s));
+                const int64_t nx = i + kPvStages - 1;  // the next tile to load
+                if (nx < nt) {
+                    if (nx >= kPvStages)
+                        ok = ptx::mbar_wait(EMPTY((int)(nx % kPvStages)), (uint32_t)((nx / kPvStages - 1) & 1),
+                                            p.wait_limit_ns, abort_flag, p.err, 50);
+                    if (!ok)
+                        break;
+                    load(nx);
+                    issued = nx + 1;
+                }
             }
             ptx::mma_commit(DONE);
             volatile int no_abort = 0;
             ptx::mbar_wait(DONE, 0, p.wait_limit_ns, &no_abort, p.err, 52);
             // copies still in flight after an abort land before the CTA exits
-            for (int64_t i = (issued > 2 ? issued - 2 : 0); i < issued; ++i)
-                ptx::mbar_wait(FULL((int)(i & 1)), (uint32_t)((i / 2) & 1), p.wait_limit_ns, &no_abort, p.err, 53);
+            for (int64_t i = (issued > kPvStages ? issued - kPvStages : 0); i < issued; ++i)
+                ptx::mbar_wait(FULL((int)(i % kPvStages)), (uint32_t)((i / kPvStages) & 1), p.wait_limit_ns, &no_abort,
+                               p.err, 53);
         }
         __syncwarp();
     } else {
@@ -413,7 +419,8 @@ cudaError_t launch_two_pass(const void *q, const void *k, const void *v, int64_t
     const uint32_t sbox[3] = {32, 128, 1};
     if (!make_f32_map_sw128(&ms, S, 3, pdims, sstrides, sbox))
         return cudaErrorInvalidValue;
-    const uint32_t smem_score = 2 * kTileBytes + 64 + 1024, smem_pv = 4 * kTileBytes + 64 + 1024;
+    const uint32_t smem_score = 2 * kTileBytes + 64 + 1024,
+                   smem_pv = 2 * kPvStages * kTileBytes + 16 * kPvStages + 32 + 1024;
     cudaError_t e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_score);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(pv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_pv);
