@@ -320,12 +320,10 @@ def host_empty(shape, dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
 
     The memory is an anonymous mapping advised for huge pages and touched, so
     that its pages exist.  If at least 90% of it landed on huge pages it is
-    registered with cudaHostRegister.  Copies from and to such a block keep
-    their rate when the host's memory is fragmented: with scattered small
-    pinned pages, concurrent copies in and out have been measured to slow
-    down by up to 2x in some steps.  Otherwise (small pages only, where a
-    registered block copies several times slower than a driver-pinned one)
-    the tensor comes from torch's pinned allocator instead.
+    registered with cudaHostRegister: a few large pages for the copy engines
+    to translate instead of many small ones.  Otherwise (small pages only,
+    where a registered block has copied several times slower than a
+    driver-pinned one) the tensor comes from torch's pinned allocator.
 
     A registered block stays registered until host_free() is called on the
     tensor (or a view of its storage), or the process exits."""
