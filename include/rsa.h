@@ -122,7 +122,9 @@ rsa_status rsa_ring_attn_workspace_size(rsa_dtype dt, int B, int H, int64_t T, i
  * out/lse for a chunk visited once); every later round computes its pairs'
  * partials and merges them; a chunk's last merge writes out (dtype dt) and
  * lse.  Requires N >= 1 and N dividing T.  `workspace` must hold
- * rsa_ring_attn_workspace_size() bytes.
+ * rsa_ring_attn_workspace_size() bytes.  The call only enqueues kernels on
+ * `stream` (no synchronisation, no allocation), so a stream capture records
+ * the whole ring as one CUDA graph that can be replayed.
  */
 rsa_status rsa_ring_attn_fwd(const void *q, const void *k, const void *v, rsa_dtype dt,
                              int B, int H, int64_t T, int d, int N, int causal,

@@ -234,3 +234,33 @@ def test_host_empty_is_page_locked_and_streams_bit_exactly():
         rsa.host_free(th)
         assert th.is_pinned() != registered
     rsa.host_free(q)  # not made by host_empty: left alone
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["merge_kernel", "fused_merge"])
+def test_ring_captures_into_a_cuda_graph_and_replays(fused):
+    # The C ABI only enqueues work on the caller's stream (no synchronisation, no
+    # allocation), so a whole ring can be captured once and replayed.
+    need_cuda()
+    B, H, T, d, N = 1, 4, 2048, 128, 4
+    (q, k, v), (qd, kd, vd) = qkv_cuda(B, H, T, d, torch.bfloat16, seed=31)
+    ref_o, ref_l = rsa.ring_attn(qd, kd, vd, N, True, fused=fused)
+    out = torch.empty_like(qd)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(rsa.workspace_size(qd.dtype, B, H, T, d, N, True, fused=fused), 1), dtype=torch.uint8,
+                     device="cuda")
+    rsa.ring_attn(qd, kd, vd, N, True, out=out, lse=lse, workspace=ws, fused=fused)  # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            rsa.ring_attn(qd, kd, vd, N, True, out=out, lse=lse, workspace=ws, fused=fused)
+    torch.cuda.current_stream().wait_stream(s)
+    out.zero_()
+    lse.zero_()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    rsa.check_device_error()
+    assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
