@@ -258,6 +258,29 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t *r)
                  : "memory");
 }
 
+
+// Thread i of the warp receives columns [col, col+64) of TMEM lane (base + i).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t *r)
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+        "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+        : RSA_R8(0), RSA_R8(8), RSA_R8(16), RSA_R8(24), RSA_R8(32), RSA_R8(40), RSA_R8(48), RSA_R8(56)
+        : "r"(taddr));
+}
+
+// The same wait for a 64-column load: all 64 registers are tied to it.
+__device__ __forceinline__ void tmem_ld_wait64(uint32_t *r)
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : RSA_U8(0), RSA_U8(8), RSA_U8(16), RSA_U8(24), RSA_U8(32), RSA_U8(40), RSA_U8(48), RSA_U8(56)
+                 :
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait_only()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");

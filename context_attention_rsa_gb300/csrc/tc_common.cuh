@@ -48,13 +48,5 @@ __device__ __forceinline__ bool softmax_bar_and(bool v)
     return r != 0;
 }
 
-// Keep uses of r[0..31] after a preceding volatile asm (the TMEM load wait).
-__device__ __forceinline__ void tie32(uint32_t *r)
-{
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-        asm volatile("" : "+r"(r[i]));
-}
-
 }  // namespace tc
 }  // namespace rsa

@@ -87,10 +87,8 @@ __device__ __forceinline__ void softmax_warps(const SoftmaxCtx &c, const BlockPa
             float mx = -INFINITY;
             if (got) {
                 ptx::tc_fence_after();
-                ptx::tmem_ld32(tS + 64 * h, s);
-                ptx::tmem_ld32(tS + 64 * h + 32, s + 32);
-                ptx::tmem_ld_wait(s);
-                tie32(s + 32);
+                ptx::tmem_ld64(tS + 64 * h, s);
+                ptx::tmem_ld_wait64(s);
                 const int64_t lim = allowed[t] - (int64_t)j * 128 - 64 * h;
                 if (lim < 64) {
 #pragma unroll
@@ -153,9 +151,9 @@ __device__ __forceinline__ void softmax_warps(const SoftmaxCtx &c, const BlockPa
             const float2 n2 = make_float2(neg, neg);
             float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                              make_float2(0.f, 0.f)};
+            uint32_t pk[32];
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-                uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int e = 32 * q + 2 * i;
@@ -163,10 +161,10 @@ __device__ __forceinline__ void softmax_warps(const SoftmaxCtx &c, const BlockPa
                     const float p0 = ptx::ex2(x.x);
                     const float p1 = ptx::ex2(x.y);
                     acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
-                    pk[i] = pack_bf16(p0, p1);
+                    pk[16 * q + i] = pack_bf16(p0, p1);
                 }
-                ptx::tmem_st16(tS + 32 * h + 16 * q, pk);
             }
+            ptx::tmem_st32(tS + 32 * h, pk);
             // P and the rescaled O complete before the MMA may read them
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
