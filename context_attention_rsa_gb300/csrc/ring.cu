@@ -451,7 +451,7 @@ rsa_status rsa_two_pass_workspace_size(rsa_dtype dt, int B, int H, int64_t T, in
         return fail(RSA_ERR_INVALID_ARG, "bytes is NULL");
     RSA_TRY(check_two_pass(dt, B, H, T, d, N));
     const size_t rows = (size_t)B * H * (size_t)(T / N);
-    *bytes = align256(rows * (size_t)T * 4) + align256(rows * (size_t)T * 2) + align256(rows * (size_t)(T / 128) * 8);
+    *bytes = align256(rows * (size_t)T * 4) + align256(rows * (size_t)T * 2) + align256(rows * (size_t)(T / 64) * 8);
     return RSA_OK;
 }
 

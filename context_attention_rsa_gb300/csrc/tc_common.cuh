@@ -1,6 +1,6 @@
-// Register-level helpers shared by the two tensor-core block-attention
-// kernels (one-SM and two-SM): bit casts, bf16 packing, three-input max, the
-// named barrier of the 256 softmax threads, and a register tie for TMEM loads.
+// Register-level helpers shared by the tensor-core kernels: bit casts, bf16
+// packing, three-input max and the named barrier of the 256 softmax threads of
+// the block-attention kernels (one-SM and two-SM).
 #pragma once
 
 #include <cuda_bf16.h>

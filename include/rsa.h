@@ -226,8 +226,8 @@ rsa_status rsa_decode_attn_fwd(const void *q, const void *k, const void *v, rsa_
  * O^n = sum_j P^n_j V_j in fp32.  Same inputs and outputs as
  * rsa_ring_attn_fwd; the workspace holds one chunk's fp32 scores and bf16
  * probabilities, B*H*(T/N)*T*6 bytes -- the O(L/N * L) memory the online
- * merge avoids -- plus per-row statistics of each 128-key score tile,
- * B*H*(T/N)*(T/128)*8 bytes (each part rounded up to 256 bytes).  Built for bf16 with d = 128 and T/N a multiple of 128
+ * merge avoids -- plus per-row statistics of each 64 keys of the row,
+ * B*H*(T/N)*(T/64)*8 bytes (each part rounded up to 256 bytes).  Built for bf16 with d = 128 and T/N a multiple of 128
  * (RSA_ERR_UNSUPPORTED otherwise).
  */
 rsa_status rsa_two_pass_workspace_size(rsa_dtype dt, int B, int H, int64_t T, int d, int N,

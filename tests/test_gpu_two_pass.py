@@ -20,6 +20,7 @@ CASES = [
     (1, 1, 384, 128, 1, True),
     (2, 2, 768, 128, 3, False),
     (1, 1, 8192, 128, 4, True),   # 64 key tiles per row: the row statistics take two strides of a warp
+    (2, 3, 2048, 128, 2, True),   # several score tiles per persistent CTA, ranges across query tiles and heads
 ]
 
 

@@ -160,8 +160,8 @@ def test_two_pass_workspace_is_quadratic():
     B, H, T, d, N = 2, 8, 4096, 128, 4
     ws = rsa.two_pass_workspace_size(torch.bfloat16, B, H, T, d, N)
     rows = B * H * (T // N)
-    # fp32 scores and bf16 probabilities of one chunk, and (max, sum) per row and 128-key tile
-    assert ws == rows * T * (4 + 2) + rows * (T // 128) * 8
+    # fp32 scores and bf16 probabilities of one chunk, and (max, sum) per row and 64 keys
+    assert ws == rows * T * (4 + 2) + rows * (T // 64) * 8
     lib = rsa.load()
     n = ctypes.c_size_t(0)
     assert lib.rsa_two_pass_workspace_size(1, 1, 1, 384, 128, 2, ctypes.byref(n)) == 2  # 192-key chunks
