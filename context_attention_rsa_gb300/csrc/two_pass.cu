@@ -35,7 +35,6 @@ namespace {
 constexpr int D = 128;
 constexpr uint32_t kBoxBytes = 128u * 128u;  // 128 rows x 128 bytes (64 bf16)
 constexpr uint32_t kTileBytes = 2 * kBoxBytes;  // 128 rows x 128 bf16
-constexpr int kThreads = 160;                   // warps 0-3 epilogue, warp 4 TMA + MMA
 
 struct TwoPassParams {
     int64_t BH, T, Tc;
@@ -433,10 +432,14 @@ __global__ void __launch_bounds__(256)
 }
 
 // O^n rows qt*128.. of head bh: sum over key chunks j in ring order (n - r) mod N
-// of P^n_j V_j, 128 keys per step, kPvStages shared-memory stages.
+// of P^n_j V_j, 128 keys per step, kPvStages shared-memory stages.  The loader
+// warp refills a stage as soon as the MMAs on it end, so every stage keeps
+// loading while the MMA warp waits (one thread doing both held the next load
+// back until the current tile had arrived).
 constexpr int kPvStages = 3;
+constexpr int kPvThreads = 192;  // warps 0-3 epilogue, warp 4 TMA loads, warp 5 MMA
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kPvThreads)
     pv_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_v,
               const __grid_constant__ TwoPassParams p)
 {
@@ -490,22 +493,35 @@ __global__ void __launch_bounds__(kThreads)
                     ptx::tma_load_3d(sv + b * kBoxBytes, &tm_v, FULL(s), b * 64, (int)kk0, (int)bh);
                 }
             };
+            // loads run as far ahead as the stages allow; the MMA warp frees them
+            int64_t issued = 0;
+            for (; issued < nt; ++issued) {
+                const int s = (int)(issued % kPvStages);
+                if (issued >= kPvStages &&
+                    !ptx::mbar_wait(EMPTY(s), (uint32_t)((issued / kPvStages - 1) & 1), p.wait_limit_ns, abort_flag,
+                                    p.err, 50))
+                    break;
+                load(issued);
+            }
+            // copies still in flight after an abort land before the CTA exits
+            volatile int no_abort = 0;
+            for (int64_t i = (issued > kPvStages ? issued - kPvStages : 0); i < issued; ++i)
+                ptx::mbar_wait(FULL((int)(i % kPvStages)), (uint32_t)((i / kPvStages) & 1), p.wait_limit_ns, &no_abort,
+                               p.err, 53);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        if (lane == 0) {
             const uint32_t idesc = ptx::idesc_bf16_f32(128, D, true);
             const uint64_t dp0 = ptx::smem_desc_sw128(base, 16, 1024);
             const uint64_t dv0 = ptx::smem_desc_sw128(base + kTileBytes, kBoxBytes, 1024);
             bool ok = true;
-            int64_t issued = 0;
-            // tile i uses stage i % kPvStages; its fill is that stage's (i / kPvStages)-th.
-            // Each step issues tile i's MMAs first and only then waits for tile
-            // i-1's to free their stage for tile i + kPvStages - 1, so the
-            // tensor core always has the next tile queued.
-            for (; issued < nt && issued < kPvStages - 1; ++issued)
-                load(issued);
             for (int64_t i = 0; ok && i < nt; ++i) {
                 const int s = (int)(i % kPvStages);
-                ok = ptx::mbar_wait(FULL(s), (uint32_t)((i / kPvStages) & 1), p.wait_limit_ns, abort_flag, p.err, 51);
-                if (!ok)
+                if (!(ok = ptx::mbar_wait(FULL(s), (uint32_t)((i / kPvStages) & 1), p.wait_limit_ns, abort_flag, p.err,
+                                          51)))
                     break;
+                ptx::tc_fence_after();
                 const uint64_t pa = dp0 + ((s * 2 * kTileBytes) >> 4);
                 const uint64_t vb = dv0 + ((s * 2 * kTileBytes) >> 4);
 #pragma unroll
@@ -514,24 +530,10 @@ __global__ void __launch_bounds__(kThreads)
                     ptx::mma_ss(tmem, pa + off, vb + ((kk * 2048) >> 4), idesc, (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 ptx::mma_commit(EMPTY(s));
-                const int64_t nx = i + kPvStages - 1;  // the next tile to load
-                if (nx < nt) {
-                    if (nx >= kPvStages)
-                        ok = ptx::mbar_wait(EMPTY((int)(nx % kPvStages)), (uint32_t)((nx / kPvStages - 1) & 1),
-                                            p.wait_limit_ns, abort_flag, p.err, 50);
-                    if (!ok)
-                        break;
-                    load(nx);
-                    issued = nx + 1;
-                }
             }
             ptx::mma_commit(DONE);
             volatile int no_abort = 0;
             ptx::mbar_wait(DONE, 0, p.wait_limit_ns, &no_abort, p.err, 52);
-            // copies still in flight after an abort land before the CTA exits
-            for (int64_t i = (issued > kPvStages ? issued - kPvStages : 0); i < issued; ++i)
-                ptx::mbar_wait(FULL((int)(i % kPvStages)), (uint32_t)((i / kPvStages) & 1), p.wait_limit_ns, &no_abort,
-                               p.err, 53);
         }
         __syncwarp();
     } else {
@@ -632,7 +634,7 @@ cudaError_t launch_two_pass(const void *q, const void *k, const void *v, int64_t
         const int64_t rows = BH * Tc;
         softmax_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
             S, static_cast<const float2 *>(stats), static_cast<__nv_bfloat16 *>(P), lse, BH, Tc, T, n);
-        pv_kernel<<<dim3((unsigned)n_qt, (unsigned)BH), kThreads, smem_pv, s>>>(mp, mv, p);
+        pv_kernel<<<dim3((unsigned)n_qt, (unsigned)BH), kPvThreads, smem_pv, s>>>(mp, mv, p);
         e = cudaGetLastError();
         if (e != cudaSuccess)
             return e;
