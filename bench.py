@@ -246,6 +246,9 @@ def main():
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip timing the ring on the ragged and million-token workloads")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--h2d-settle-gbs", type=float, default=150.0,
+                    help="before the e2e timed loop, wait for a host-to-device probe this fast")
+    ap.add_argument("--h2d-settle-s", type=float, default=90.0, help="longest wait for that probe")
     ap.add_argument("--shape", default=None,
                     help="B,H,T,d,N,causal: a bf16 normal-recipe workload instead of --workload (profiling)")
     args = ap.parse_args()
@@ -473,16 +476,27 @@ def main():
         _, _, bufs = rsa.ring_attn_from_host(qh, kh, vh, N, causal, device=dev)  # warm-up
         rsa.ring_attn_from_host(qh, kh, vh, N, causal, device=dev, buffers=bufs)
         torch.cuda.synchronize()
-        # host-to-device bandwidth just before the timed loop: one copy of Q's
-        # pinned host buffer (the link is shared with other work on the host)
+        # Host-to-device bandwidth just before the timed loop: one copy of Q's
+        # pinned host buffer.  Right after another large process on the host has
+        # exited, such copies have run at 17-47 GB/s for a minute or so before
+        # returning to ~211 GB/s, so the probe is repeated every 5 s, for at most
+        # --h2d-settle-s seconds, until it reaches --h2d-settle-gbs.  Every probe
+        # and the time waited go into the output line.
         probe = torch.empty_like(qh, device=dev)
-        p0 = torch.cuda.Event(enable_timing=True)
-        p1 = torch.cuda.Event(enable_timing=True)
-        p0.record(stream)
-        probe.copy_(qh, non_blocking=True)
-        p1.record(stream)
-        torch.cuda.synchronize()
-        h2d_probe = qh.numel() * qh.element_size() / (p0.elapsed_time(p1) * 1e-3) / 1e9
+        settle, t_settle = [], time.time()
+        while True:
+            p0 = torch.cuda.Event(enable_timing=True)
+            p1 = torch.cuda.Event(enable_timing=True)
+            p0.record(stream)
+            probe.copy_(qh, non_blocking=True)
+            p1.record(stream)
+            torch.cuda.synchronize()
+            h2d_probe = qh.numel() * qh.element_size() / (p0.elapsed_time(p1) * 1e-3) / 1e9
+            settle.append(round(h2d_probe, 1))
+            if h2d_probe >= args.h2d_settle_gbs or time.time() - t_settle >= args.h2d_settle_s:
+                break
+            time.sleep(5.0)
+        settle_s = time.time() - t_settle
         del probe
         e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
         barrier()
@@ -503,6 +517,10 @@ def main():
         e2e = {"value": whole_job_tflops(flops, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "step_ms": [round(x, 2) for x in e_steps], "clocks": e_clk,
                "h2d_gbs_before": round(h2d_probe, 1),
+               "h2d_settle": {"probes_gbs": settle, "waited_s": round(settle_s, 1),
+                              "target_gbs": args.h2d_settle_gbs, "limit_s": args.h2d_settle_s},
+               "host_buffers": {name: rsa.host_kind(t) for name, t in
+                                (("q", qh), ("k", kh), ("v", vh), ("out", bufs["out_host"]), ("lse", bufs["lse_host"]))},
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         k_cpu, v_cpu, q_cpu = kh, vh, qh
     else:

@@ -27,7 +27,7 @@ from . import _build
 __all__ = [
     "RsaError", "load", "library_path", "block_attn_fwd", "merge", "merge_finalize",
     "ring_attn", "ring_attn_noalloc", "ring_attn_timed", "decode_attn", "decode_workspace_size",
-    "two_pass_attn", "two_pass_workspace_size", "ring_attn_from_host", "slab_plan", "host_empty", "host_free",
+    "two_pass_attn", "two_pass_workspace_size", "ring_attn_from_host", "slab_plan", "host_empty", "host_kind", "host_free",
     "workspace_size", "ring_schedule", "set_block_kernel",
     "set_wait_limit_ns", "check_device_error", "selftest_wait_timeout", "version",
     "RSA_F32", "RSA_BF16",
@@ -351,6 +351,16 @@ def host_empty(shape, dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
         except BufferError:
             pass  # closed when the last reference goes
     return torch.empty(shape, dtype=dtype, pin_memory=True)
+
+
+def host_kind(t: torch.Tensor) -> str:
+    """How a host tensor's memory is held: "registered-huge" (a host_empty
+    block on huge pages, registered with cudaHostRegister), "pinned" (torch's
+    page-locked allocator) or "pageable"."""
+    with _host_lock:
+        if t.untyped_storage().data_ptr() in _host_blocks:
+            return "registered-huge"
+    return "pinned" if t.is_pinned() else "pageable"
 
 
 def host_free(t: torch.Tensor) -> None:

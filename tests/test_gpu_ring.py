@@ -230,9 +230,13 @@ def test_host_empty_is_page_locked_and_streams_bit_exactly():
     for th in (qh, kh, vh):
         # a block on huge pages is registered by host_empty and unregistered by
         # host_free; otherwise it came from torch's pinned allocator
+        kind = rsa.host_kind(th)
+        assert kind in ("registered-huge", "pinned")
         registered = th.untyped_storage().data_ptr() in rsa._host_blocks
+        assert registered == (kind == "registered-huge")
         rsa.host_free(th)
         assert th.is_pinned() != registered
+    assert rsa.host_kind(q) == "pageable"
     rsa.host_free(q)  # not made by host_empty: left alone
 
 
