@@ -1,7 +1,8 @@
 """The benchmark's output contract, checked on the CPU through its reference
 arm (the oracle timed on a bounded sample): one JSON line with the keys the
 measurement is read from.  The GPU arm prints the same keys plus the
-roofline, clocks and per-section results; its run is covered on a GPU."""
+roofline, clocks and per-section results; test_gpu_bench_line.py checks it on
+a GPU."""
 import json
 import os
 import subprocess
