@@ -7,6 +7,13 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+# The mutation test (test_oracle_mutations.py) reruns the oracle's pin tests
+# against a copy of the oracle with one planted mistake: this variable names
+# the folder holding that copy, which then shadows the real package.
+_ORACLE_UNDER_TEST = os.environ.get("RSA_ORACLE_UNDER_TEST")
+if _ORACLE_UNDER_TEST:
+    sys.path.insert(0, _ORACLE_UNDER_TEST)
+
 GOLDEN = os.path.join(ROOT, "tests", "golden")
 
 
