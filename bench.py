@@ -238,7 +238,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="rsa", choices=["rsa", "reference"])
     ap.add_argument("--workload", default="page1_causal_bf16")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fused", action="store_true", help="skip timing the fused-merge ring variant")
     ap.add_argument("--no-decode", action="store_true", help="skip timing decode on the million-token cache")
@@ -295,8 +295,7 @@ def main():
     torch.cuda.synchronize()
     rsa.check_device_error()
 
-    ev0 = [[torch.cuda.Event(enable_timing=True) for _ in range(n_launch)] for _ in range(args.steps)]
-    ev1 = [[torch.cuda.Event(enable_timing=True) for _ in range(n_launch)] for _ in range(args.steps)]
+    # The headline: K plain rsa_ring_attn_fwd calls, nothing else in the timed region.
     t_start = torch.cuda.Event(enable_timing=True)
     t_stop = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -304,9 +303,8 @@ def main():
     barrier()
     torch.cuda.synchronize()
     t_start.record(stream)
-    kinds = None
     for s in range(args.steps):
-        kinds = rsa.ring_attn_timed(q, k, v, N, causal, out, lse, ws, ev0[s], ev1[s])
+        rsa.ring_attn(q, k, v, N, causal, out=out, lse=lse, workspace=ws)
     t_stop.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -314,6 +312,17 @@ def main():
     rsa.check_device_error()
     ms_total = max_over_ranks(pg, t_start.elapsed_time(t_stop), dev)
     ms_step = ms_total / args.steps
+
+    # Per-kernel breakdown, in a separate loop: the same ring with CUDA events
+    # recorded around each launch on the launching stream.
+    ev0 = [[torch.cuda.Event(enable_timing=True) for _ in range(n_launch)] for _ in range(args.steps)]
+    ev1 = [[torch.cuda.Event(enable_timing=True) for _ in range(n_launch)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    kinds = None
+    for s in range(args.steps):
+        kinds = rsa.ring_attn_timed(q, k, v, N, causal, out, lse, ws, ev0[s], ev1[s])
+    torch.cuda.synchronize()
+    rsa.check_device_error()
 
     blk_ms = sum(ev0[s][i].elapsed_time(ev1[s][i]) for s in range(args.steps) for i in range(n_launch)
                  if kinds[i] == 0) / args.steps
@@ -464,7 +473,7 @@ def main():
             del qo, ko, vo, oo, lo, wso
             torch.cuda.empty_cache()
 
-    # ---- end to end from pinned host memory (public API) --------------------
+    # ---- end to end from host memory (public API, rsa_ring_attn_fwd_host) ----
     e2e = None
     if args.e2e_steps > 0:
         qh, kh, vh = (rsa.host_empty(t.shape, t.dtype) for t in (q, k, v))
@@ -472,16 +481,15 @@ def main():
             th.copy_(td)
         del q, k, v, out, lse, ws
         torch.cuda.empty_cache()
-        bufs = None
-        _, _, bufs = rsa.ring_attn_from_host(qh, kh, vh, N, causal, device=dev)  # warm-up
-        rsa.ring_attn_from_host(qh, kh, vh, N, causal, device=dev, buffers=bufs)
+        bufs = {}
+        for _ in range(2):  # warm-up: the library's copy streams, the workspace, the host outputs
+            rsa.ring_attn_from_host(qh, kh, vh, N, causal, device=dev, buffers=bufs)
         torch.cuda.synchronize()
         # Host-to-device bandwidth just before the timed loop: one copy of Q's
-        # pinned host buffer.  Right after another large process on the host has
-        # exited, such copies have run at 17-47 GB/s for a minute or so before
-        # returning to ~211 GB/s, so the probe is repeated every 5 s, for at most
-        # --h2d-settle-s seconds, until it reaches --h2d-settle-gbs.  Every probe
-        # and the time waited go into the output line.
+        # host buffer.  Such copies have run far below their usual ~211 GB/s on
+        # some boxes; the probe is repeated every 5 s, for at most
+        # --h2d-settle-s seconds, until it reaches --h2d-settle-gbs.  Every
+        # probe and the time waited go into the output line.
         probe = torch.empty_like(qh, device=dev)
         settle, t_settle = [], time.time()
         while True:
@@ -498,6 +506,11 @@ def main():
             time.sleep(5.0)
         settle_s = time.time() - t_settle
         del probe
+        torch.cuda.empty_cache()
+        # which host pages are huge right before the timed loop (copies from
+        # base-page parts of a block have run far slower)
+        host_before = {name: rsa.host_info(t) for name, t in
+                       (("q", qh), ("k", kh), ("v", vh), ("out+lse", bufs["out_host"]))}
         e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
         barrier()
         torch.cuda.synchronize()
@@ -515,12 +528,15 @@ def main():
         h2d = 3 * qh.numel() * qh.element_size()
         d2h = bufs["out_host"].numel() * bufs["out_host"].element_size() + bufs["lse_host"].numel() * 4
         e2e = {"value": whole_job_tflops(flops, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
+               "call": "rsa_ring_attn_fwd_host", "steps": args.e2e_steps,
                "step_ms": [round(x, 2) for x in e_steps], "clocks": e_clk,
                "h2d_gbs_before": round(h2d_probe, 1),
                "h2d_settle": {"probes_gbs": settle, "waited_s": round(settle_s, 1),
                               "target_gbs": args.h2d_settle_gbs, "limit_s": args.h2d_settle_s},
-               "host_buffers": {name: rsa.host_kind(t) for name, t in
-                                (("q", qh), ("k", kh), ("v", vh), ("out", bufs["out_host"]), ("lse", bufs["lse_host"]))},
+               "host_buffers": host_before,
+               "host_buffers_after": {name: rsa.host_info(t) for name, t in
+                                      (("q", qh), ("k", kh), ("v", vh), ("out+lse", bufs["out_host"]))},
+               "slabs": rsa.slab_plan(B * H),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         k_cpu, v_cpu, q_cpu = kh, vh, qh
     else:

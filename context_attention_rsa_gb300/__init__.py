@@ -14,9 +14,7 @@ softmax seems to require all attention scores at once") and causal skipping
 """
 from __future__ import annotations
 
-import atexit
 import ctypes
-import mmap
 import threading
 from typing import List, Optional, Sequence, Tuple
 
@@ -27,7 +25,8 @@ from . import _build
 __all__ = [
     "RsaError", "load", "library_path", "block_attn_fwd", "merge", "merge_finalize",
     "ring_attn", "ring_attn_noalloc", "ring_attn_timed", "decode_attn", "decode_workspace_size",
-    "two_pass_attn", "two_pass_workspace_size", "ring_attn_from_host", "slab_plan", "host_empty", "host_kind", "host_free",
+    "two_pass_attn", "two_pass_workspace_size", "ring_attn_from_host", "slab_plan", "host_empty", "host_kind",
+    "host_info", "host_workspace_size",
     "workspace_size", "ring_schedule", "set_block_kernel",
     "set_wait_limit_ns", "check_device_error", "selftest_wait_timeout", "version",
     "RSA_F32", "RSA_BF16",
@@ -83,8 +82,22 @@ _SIGS = {
                             _c_void_p, _c_void_p, _c_void_p, ctypes.c_size_t, _c_void_p],
     "rsa_ring_schedule": [_i32, _i32, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _i32,
                           ctypes.POINTER(_i32)],
+    "rsa_block_attn_fold": [_c_void_p, _i64, _c_void_p, _c_void_p, _i64, _i32, _i32, _i32, _i32, _i64, _i64, _i64,
+                            _i64, _i64, _i64, _i32, _i32, _c_void_p, _c_void_p, _c_void_p, _c_void_p],
+    "rsa_rank_ring_plan": [_i32, _i32, _i64, _i32, _i32, ctypes.POINTER(_i64), _i32, ctypes.POINTER(_i32)],
+    "rsa_host_alloc": [ctypes.c_size_t, ctypes.POINTER(_c_void_p)],
+    "rsa_host_free": [_c_void_p],
+    "rsa_host_info": [_c_void_p, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t),
+                      ctypes.POINTER(_i32)],
+    "rsa_host_slab_plan": [_i32, _i32, _i32, ctypes.POINTER(_i32), _i32, ctypes.POINTER(_i32)],
+    "rsa_ring_attn_host_workspace_size": [_i32, _i32, _i32, _i64, _i32, _i32, _i32,
+                                          ctypes.POINTER(ctypes.c_size_t)],
+    "rsa_ring_attn_fwd_host": [_c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _i64, _i32, _i32, _i32,
+                               _c_void_p, _c_void_p, _c_void_p, ctypes.c_size_t, _c_void_p],
     "rsa_set_wait_limit_ns": [ctypes.c_uint64],
     "rsa_set_block_kernel": [_i32],
+    "rsa_debug_inject_launch_failure": [_i32],
+    "rsa_debug_checks": [],
     "rsa_check_device_error": [_c_void_p],
     "rsa_selftest_wait_timeout": [_c_void_p],
     "rsa_status_string": [_i32],
@@ -93,12 +106,23 @@ _SIGS = {
 }
 
 
+def debug_variant() -> bool:
+    """True when the environment asks for the RSA_DEBUG build (RSA_DEBUG=1):
+    kernels with device-side bounds checks, reported by check_device_error."""
+    import os
+    return os.environ.get("RSA_DEBUG", "0") not in ("", "0")
+
+
 def library_path(build: bool = True) -> str:
-    return _build.build() if build else _build.LIB
+    dbg = debug_variant()
+    if build:
+        return _build.build(debug=dbg)
+    return _build.DEBUG_LIB if dbg else _build.LIB
 
 
 def load(build: bool = True):
-    """Load librsa.so (building it in-tree first if it is stale)."""
+    """Load librsa.so (building it in-tree first if it is stale); the
+    RSA_DEBUG variant when the environment sets RSA_DEBUG=1."""
     global _lib
     with _lock:
         if _lib is None:
@@ -109,6 +133,8 @@ def load(build: bool = True):
                 fn.argtypes = args
                 fn.restype = ctypes.c_char_p if name in ("rsa_status_string", "rsa_last_error_string") \
                     else ctypes.c_int
+            if bool(lib.rsa_debug_checks()) != debug_variant():
+                raise RsaError("load", 2, f"{path} does not match RSA_DEBUG={int(debug_variant())}")
             _lib = lib
     return _lib
 
@@ -201,14 +227,26 @@ def merge(o_acc: torch.Tensor, lse_acc: torch.Tensor, o_blk: torch.Tensor, lse_b
 
 def merge_finalize(o_acc, lse_acc, o_blk, lse_blk, out_dtype=torch.bfloat16, out=None, lse_out=None,
                    stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The last merge of a ring: merge((o_acc, lse_acc), (o_blk, lse_blk))
+    written to (out [o_acc's shape, out_dtype], lse_out fp32); the
+    accumulator is only read."""
     d = o_acc.shape[-1]
     rows = lse_acc.numel()
+    if o_acc.dtype != torch.float32 or lse_acc.dtype != torch.float32 or lse_blk.dtype != torch.float32:
+        raise TypeError("o_acc, lse_acc and lse_blk must be float32")
     if o_blk.numel() != rows * d or o_acc.numel() != rows * d or lse_blk.numel() != rows:
         raise ValueError("row counts differ")
     if out is None:
         out = torch.empty(o_acc.shape, dtype=out_dtype, device=o_acc.device)
     if lse_out is None:
         lse_out = torch.empty(lse_acc.shape, dtype=torch.float32, device=o_acc.device)
+    if out.dtype != out_dtype or out.numel() != rows * d:
+        raise ValueError("out must hold rows x d values of out_dtype")
+    if lse_out.dtype != torch.float32 or lse_out.numel() != rows:
+        raise ValueError("lse_out must hold one float32 per row")
+    for t in (o_acc, lse_acc, o_blk, lse_blk, out, lse_out):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("merge operands must be contiguous CUDA tensors")
     _call("rsa_merge_finalize", o_acc.data_ptr(), lse_acc.data_ptr(), o_blk.data_ptr(), _dt(o_blk),
           lse_blk.data_ptr(), rows, d, out.data_ptr(), _dt(out), lse_out.data_ptr(), _stream(stream))
     return out, lse_out
@@ -291,201 +329,127 @@ def ring_launch_count(N: int, causal: bool, fused: bool = False) -> int:
     return n
 
 
-# Page-locked host blocks made by host_empty: storage address -> (mmap, bytes, base tensor).
+# Host blocks made by host_empty: block address -> bytes.  A block is freed
+# (rsa_host_free) when the last tensor viewing it is garbage-collected.
 _host_blocks = {}
 _host_lock = threading.Lock()
 
+RSA_HOST_HUGE = 1
+RSA_HOST_PINNED = 2
 
-def _huge_bytes(addr: int) -> int:
-    """Bytes of the mapping that contains addr that sit on transparent huge
-    pages (AnonHugePages in /proc/self/smaps); 0 if it cannot be read."""
-    try:
-        with open("/proc/self/smaps") as f:
-            inside = False
-            for line in f:
-                head = line.split(None, 1)[0]
-                if "-" in head and ":" not in head:
-                    lo, hi = (int(x, 16) for x in head.split("-"))
-                    inside = lo <= addr < hi
-                elif inside and head == "AnonHugePages:":
-                    return int(line.split()[1]) * 1024
-    except (OSError, ValueError):
-        pass
-    return 0
+
+def _release_host_block(ptr: int) -> None:
+    with _host_lock:
+        known = _host_blocks.pop(ptr, None) is not None
+    if known and _lib is not None:
+        _lib.rsa_host_free(ptr)
 
 
 def host_empty(shape, dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
-    """A page-locked host tensor for streaming copies, on transparent huge
-    pages where the host can provide them.
-
-    The memory is an anonymous mapping advised for huge pages and touched, so
-    that its pages exist.  If at least 90% of it landed on huge pages it is
-    registered with cudaHostRegister: a few large pages for the copy engines
-    to translate instead of many small ones.  Otherwise (small pages only,
-    where a registered block has copied several times slower than a
-    driver-pinned one) the tensor comes from torch's pinned allocator.
-
-    A registered block stays registered until host_free() is called on the
-    tensor (or a view of its storage), or the process exits."""
+    """A page-locked host tensor for streaming copies, from rsa_host_alloc:
+    memory on transparent huge pages registered with the CUDA driver (or
+    driver-pinned memory where huge pages are not to be had).  Copies from
+    base-page pinned memory have been measured to slow down after the memory
+    sat idle; huge-page memory kept its speed.  The block is released when the
+    last tensor viewing it is gone."""
+    import weakref
     shape = tuple(int(x) for x in shape)
     numel = 1
     for x in shape:
         numel *= x
-    nbytes = numel * torch.empty((), dtype=dtype).element_size()
-    size = max(1, (nbytes + (2 << 20) - 1) // (2 << 20)) * (2 << 20)
-    if hasattr(mmap, "MADV_HUGEPAGE"):
-        m = mmap.mmap(-1, size, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS, prot=mmap.PROT_READ | mmap.PROT_WRITE)
-        m.madvise(mmap.MADV_HUGEPAGE)
-        raw = torch.frombuffer(m, dtype=torch.uint8, count=size)
-        raw.fill_(0)
-        if _huge_bytes(raw.data_ptr()) >= 0.9 * size:
-            err = torch.cuda.cudart().cudaHostRegister(raw.data_ptr(), size, 0)
-            if int(err) != 0:
-                raise RsaError("host_empty", 3, f"cudaHostRegister of {size} bytes failed: {err}")
-            with _host_lock:
-                _host_blocks[raw.data_ptr()] = (m, size, raw)
-            return raw[:nbytes].view(dtype).view(shape)
-        del raw
-        try:
-            m.close()
-        except BufferError:
-            pass  # closed when the last reference goes
-    return torch.empty(shape, dtype=dtype, pin_memory=True)
+    nbytes = max(1, numel * torch.empty((), dtype=dtype).element_size())
+    ptr = ctypes.c_void_p(0)
+    _call("rsa_host_alloc", nbytes, ctypes.byref(ptr))
+    addr = int(ptr.value)
+    buf = (ctypes.c_uint8 * nbytes).from_address(addr)
+    with _host_lock:
+        _host_blocks[addr] = nbytes
+    weakref.finalize(buf, _release_host_block, addr)
+    raw = torch.frombuffer(buf, dtype=torch.uint8, count=nbytes)
+    return raw[:numel * torch.empty((), dtype=dtype).element_size()].view(dtype).view(shape)
+
+
+def host_info(t: torch.Tensor) -> dict:
+    """rsa_host_info of a tensor made by host_empty: usable bytes, bytes the
+    kernel backs with huge pages now, and kind ("registered-huge" or
+    "pinned")."""
+    ptr = t.untyped_storage().data_ptr()
+    n, huge, kind = ctypes.c_size_t(0), ctypes.c_size_t(0), ctypes.c_int(0)
+    _call("rsa_host_info", ptr, ctypes.byref(n), ctypes.byref(huge), ctypes.byref(kind))
+    return {"bytes": int(n.value), "huge_bytes": int(huge.value),
+            "kind": "registered-huge" if kind.value == RSA_HOST_HUGE else "pinned"}
 
 
 def host_kind(t: torch.Tensor) -> str:
-    """How a host tensor's memory is held: "registered-huge" (a host_empty
-    block on huge pages, registered with cudaHostRegister), "pinned" (torch's
-    page-locked allocator) or "pageable"."""
+    """How a host tensor's memory is held: "registered-huge" or "pinned" (a
+    host_empty block), "pinned" (torch's page-locked allocator) or
+    "pageable"."""
     with _host_lock:
-        if t.untyped_storage().data_ptr() in _host_blocks:
-            return "registered-huge"
+        ours = t.untyped_storage().data_ptr() in _host_blocks
+    if ours:
+        return host_info(t)["kind"]
     return "pinned" if t.is_pinned() else "pageable"
 
 
-def host_free(t: torch.Tensor) -> None:
-    """Unregister a block made by host_empty (the memory itself goes away with
-    its last tensor).  Tensors not made by host_empty are left alone."""
-    ptr = t.untyped_storage().data_ptr()
-    with _host_lock:
-        blk = _host_blocks.pop(ptr, None)
-    if blk is not None:
-        torch.cuda.cudart().cudaHostUnregister(ptr)
-
-
-@atexit.register
-def _host_free_all():
-    with _host_lock:
-        ptrs = list(_host_blocks)
-        _host_blocks.clear()
-    for ptr in ptrs:
-        try:
-            torch.cuda.cudart().cudaHostUnregister(ptr)
-        except Exception:
-            pass
-
-
 def slab_plan(BH: int, groups: int = 8, ramp: bool = True) -> List[int]:
-    """Heads per slab for ring_attn_from_host.
-
-    Without ramp: `groups` equal slabs.  With ramp: slabs of at most
-    ceil(BH / groups) heads in the middle, preceded by slabs that grow about
-    1.6x at a time from an eighth of that, and followed by slabs that shrink
-    back to an eighth.  Copying one head in takes less time than computing it,
-    so each slab's copy hides under its predecessor's ring.  What is left
-    exposed is the first slab's copy in and the last slab's copy out, and the
-    ramps keep those small."""
+    """Heads per slab of the host-streaming path (rsa_host_slab_plan): about
+    `groups` slabs of at most ceil(BH / groups) heads; with ramp, small slabs
+    that grow about 1.6x at a time lead in and shrinking ones lead out, so
+    each slab's copy hides under its predecessor's ring."""
     if BH <= 0:
         return []
-    cap = max(1, -(-BH // max(1, min(int(groups), BH))))
-    if not ramp or cap < 8:
-        n = -(-BH // cap)
-        return [cap] * (BH // cap) + ([BH % cap] if BH % cap else []) if n > 0 else []
-    up, x = [], max(1, cap // 8)
-    while x < cap:
-        up.append(x)
-        x = max(x + 1, (x * 8) // 5)
-    down = [max(1, cap // 2), max(1, cap // 4), max(1, cap // 8)]
-    if sum(up) + sum(down) >= BH:
-        return slab_plan(BH, groups, ramp=False)
-    mid = BH - sum(up) - sum(down)
-    k = -(-mid // cap)  # middle slabs, as equal as possible
-    middle = [mid // k + (1 if i < mid % k else 0) for i in range(k)]
-    return up + middle + down
+    cap = max(8, BH)
+    slabs = (ctypes.c_int * cap)()
+    n = ctypes.c_int(0)
+    _call("rsa_host_slab_plan", int(BH), int(groups), int(bool(ramp)), slabs, cap, ctypes.byref(n))
+    return [slabs[i] for i in range(n.value)]
+
+
+def host_workspace_size(dtype: torch.dtype, B: int, H: int, T: int, d: int, N: int, causal: bool) -> int:
+    n = ctypes.c_size_t(0)
+    dt = RSA_F32 if dtype == torch.float32 else RSA_BF16
+    _call("rsa_ring_attn_host_workspace_size", dt, B, H, T, d, N, int(bool(causal)), ctypes.byref(n))
+    return int(n.value)
 
 
 def ring_attn_from_host(q_host, k_host, v_host, N: int, causal: bool, device=None, stream=None,
-                        buffers=None, groups: int = 8, ramp: bool = True):
-    """End-to-end call from host memory: Q, K, V (host tensors, ideally made
-    by host_empty) in, out and lse (page-locked host tensors) back.
-
-    Heads are independent problems, so the B*H heads are cut into slabs
-    (slab_plan(B*H, groups, ramp)) that stream through three CUDA streams: the
-    copy of slab g+1 to the device, the ring on slab g (C ABI, on ``stream``
-    or the current stream) and the copy of slab g-1 back to the host all
-    overlap.  Device slabs are double-buffered.  The returned host tensors are
-    complete once ``stream`` has passed the call (it waits for the last copy
-    back).  ``buffers`` (a dict, filled on first use) keeps the device slabs,
-    the workspace, the pinned outputs and the copy streams for reuse."""
+                        buffers=None):
+    """End-to-end call from host memory (rsa_ring_attn_fwd_host): Q, K, V host
+    tensors [B, H, T, d] in (ideally made by host_empty), out and lse back in
+    page-locked host tensors.  The C library streams slabs of heads through
+    the GPU, overlapping the copies in and out with the ring.  The returned
+    host tensors are complete once ``stream`` (default: the current stream)
+    has passed the call.  ``buffers`` (a dict, filled on first use) keeps the
+    device workspace and the host outputs for reuse."""
     dev = torch.device(device) if device is not None else torch.device("cuda")
     b = buffers if buffers is not None else {}
+    for name, t in (("q", q_host), ("k", k_host), ("v", v_host)):
+        if t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, H, T, d] host tensor")
+    if not (q_host.shape == k_host.shape == v_host.shape and q_host.dtype == k_host.dtype == v_host.dtype):
+        raise ValueError("q, k, v must share shape and dtype")
     B, H, T, d = q_host.shape
-    BH = B * H
-    plan = slab_plan(BH, groups, ramp)
-    hg = max(plan)  # heads in the largest slab
-    main = torch.cuda.current_stream(dev) if stream is None else stream
-    key = (tuple(q_host.shape), q_host.dtype, N, bool(causal), tuple(plan), str(dev))
+    key = (tuple(q_host.shape), q_host.dtype, N, bool(causal), str(dev))
     if b.get("key") != key:
-        for name in ("out_host", "lse_host"):
-            if name in b:
-                host_free(b[name])
         b.clear()
         b["key"] = key
-        mk = lambda *shape, dt=q_host.dtype: torch.empty(shape, dtype=dt, device=dev)
-        b["in"] = [[mk(hg, T, d) for _ in range(3)] for _ in range(2)]
-        b["out"] = [mk(hg, T, d) for _ in range(2)]
-        b["lse"] = [mk(hg, T, dt=torch.float32) for _ in range(2)]
-        b["ws"] = mk(max(workspace_size(q_host.dtype, 1, hg, T, d, N, causal), 1), dt=torch.uint8)
-        b["out_host"] = host_empty(q_host.shape, q_host.dtype)
-        b["lse_host"] = host_empty((B, H, T), torch.float32)
-        b["s_in"] = torch.cuda.Stream(dev)
-        b["s_out"] = torch.cuda.Stream(dev)
-    s_in, s_out = b["s_in"], b["s_out"]
-    src = [t.reshape(BH, T, d) for t in (q_host, k_host, v_host)]
-    oh = b["out_host"].view(BH, T, d)
-    lh = b["lse_host"].view(BH, T)
-    s_in.wait_stream(main)
-    s_out.wait_stream(main)
-    ev_comp, ev_out = [], []
-    h0 = 0
-    for g, n in enumerate(plan):
-        h1 = h0 + n
-        slot = g % 2
-        with torch.cuda.stream(s_in):
-            if g >= 2:
-                s_in.wait_event(ev_comp[g - 2])  # ring on slab g-2 has read this slot
-            for t_dev, t_host in zip(b["in"][slot], src):
-                t_dev[:n].copy_(t_host[h0:h1], non_blocking=True)
-            ev_in = torch.cuda.Event()
-            ev_in.record(s_in)
-        main.wait_event(ev_in)
-        if g >= 2:
-            main.wait_event(ev_out[g - 2])  # slab g-2 has been copied out of this slot
-        qd, kd, vd = (t[:n].view(1, n, T, d) for t in b["in"][slot])
-        ring_attn(qd, kd, vd, N, causal, out=b["out"][slot][:n].view(1, n, T, d),
-                  lse=b["lse"][slot][:n].view(1, n, T), workspace=b["ws"], stream=main)
-        ev = torch.cuda.Event()
-        ev.record(main)
-        ev_comp.append(ev)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev)
-            oh[h0:h1].copy_(b["out"][slot][:n], non_blocking=True)
-            lh[h0:h1].copy_(b["lse"][slot][:n], non_blocking=True)
-            ev = torch.cuda.Event()
-            ev.record(s_out)
-            ev_out.append(ev)
-        h0 = h1
-    main.wait_event(ev_out[-1])
+        with torch.cuda.device(dev):
+            b["ws"] = torch.empty(host_workspace_size(q_host.dtype, B, H, T, d, N, causal) + 256,
+                                  dtype=torch.uint8, device=dev)
+        # out and lse share one huge-page block
+        esz = q_host.element_size()
+        out_bytes = B * H * T * d * esz
+        lse_off = (out_bytes + 255) // 256 * 256
+        blk = host_empty((lse_off + B * H * T * 4,), torch.uint8)
+        b["out_host"] = blk[:out_bytes].view(q_host.dtype).view(B, H, T, d)
+        b["lse_host"] = blk[lse_off:].view(torch.float32).view(B, H, T)
+    ws = b["ws"]
+    ws_ptr = (ws.data_ptr() + 255) // 256 * 256
+    st = torch.cuda.current_stream(dev) if stream is None else stream
+    with torch.cuda.device(dev):
+        _call("rsa_ring_attn_fwd_host", q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(), _dt(q_host),
+              B, H, T, d, N, int(bool(causal)), b["out_host"].data_ptr(), b["lse_host"].data_ptr(), ws_ptr,
+              ws.numel() - (ws_ptr - ws.data_ptr()), _stream(st))
     return b["out_host"], b["lse_host"], b
 
 
@@ -568,6 +532,12 @@ def set_block_kernel(which: str) -> None:
     one-SM kernel), "one_sm", or "two_sm" (the CTA-pair kernel where it
     applies: d = 128, pairs of at least 512 rows, no key splits)."""
     _call("rsa_set_block_kernel", BLOCK_KERNELS[which])
+
+
+def inject_launch_failure(countdown: int) -> None:
+    """Make the library's launch after the next `countdown` ones report a
+    launch failure (RSA_ERR_CUDA) instead of launching; negative: off."""
+    _call("rsa_debug_inject_launch_failure", int(countdown))
 
 
 def check_device_error(stream=None) -> None:

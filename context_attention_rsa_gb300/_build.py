@@ -20,6 +20,11 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "librsa.so")
 STAMP = os.path.join(BUILD, "librsa.stamp")
+# The RSA_DEBUG variant: device-side bounds checks on the kernels' computed
+# global accesses, which record the first bad index into the device error
+# word (no trap) and skip the access.
+DEBUG_BUILD = os.path.join(BUILD, "debug")
+DEBUG_LIB = os.path.join(DEBUG_BUILD, "librsa.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -55,20 +60,25 @@ def _digest(extra_flags) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile librsa.so if stale; returns its path.  Raises on failure."""
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile librsa.so (or, with debug, its RSA_DEBUG variant) if stale;
+    returns its path.  Raises on failure."""
+    out_dir, lib = (DEBUG_BUILD, DEBUG_LIB) if debug else (BUILD, LIB)
+    stamp = os.path.join(out_dir, "librsa.stamp")
+    if debug:
+        extra_flags = ["-DRSA_DEBUG=1", *extra_flags]
     with _lock:
-        os.makedirs(BUILD, exist_ok=True)
+        os.makedirs(out_dir, exist_ok=True)
         dig = _digest(extra_flags)
-        if not force and os.path.exists(LIB) and os.path.exists(STAMP):
-            with open(STAMP) as f:
+        if not force and os.path.exists(lib) and os.path.exists(stamp):
+            with open(stamp) as f:
                 if f.read().strip() == dig:
-                    return LIB
+                    return lib
         cc = nvcc()
         objs = []
         cmds = []
         for src in sources():
-            obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+            obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
             objs.append(obj)
             cmds.append([cc, *ARCH, *NVCC_FLAGS, *extra_flags, "-I", INCLUDE, "-c", src, "-o", obj])
 
@@ -83,15 +93,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
                 print(r.stdout + r.stderr)
             if r.returncode != 0:
                 raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
-        tmp = LIB + f".tmp{os.getpid()}"
+        tmp = lib + f".tmp{os.getpid()}"
         link = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart=static"]
         r = subprocess.run(link, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + " ".join(link) + "\n" + r.stdout + r.stderr)
-        os.replace(tmp, LIB)
-        with open(STAMP, "w") as f:
+        os.replace(tmp, lib)
+        with open(stamp, "w") as f:
             f.write(dig)
-        return LIB
+        return lib
 
 
 if __name__ == "__main__":

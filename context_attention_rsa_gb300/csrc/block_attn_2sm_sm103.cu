@@ -111,7 +111,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int pi = (int)(unit % p.npairs);
     const int bh = (int)(unit / p.npairs);
     const PairDesc &pr = p.pairs[pi];
-    const int64_t kv_off = pr.kv_off;
+    const int64_t kv_off = pr.kv_off;    // global position (mask)
+    const int64_t kv_row = pr.kv_row0;   // row in the K/V tensors
     const int64_t kv_len = p.kv_len;
     const int64_t qc0 = (int64_t)qg * 512;               // first row of the cluster
     const int64_t rows_valid = min((int64_t)512, p.q_len - qc0);
@@ -169,7 +170,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (use > 0 &&
                     !ptx::mbar_wait(BAR(C::kKVE + slot), (use - 1) & 1, lim_ns, abort_flag, p.err, 1))
                     break;
-                const int row = (int)(kv_off + (int64_t)(ld >> 1) * 128);
+                const int row = (int)(kv_row + (int64_t)(ld >> 1) * 128);
                 const uint32_t dst = sKV + slot * C::kStageBytes;
                 if (leader)
                     ptx::mbar_arrive_expect_tx(BAR(C::kKVF + slot), 2 * C::kStageBytes);

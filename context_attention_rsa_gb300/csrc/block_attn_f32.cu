@@ -56,9 +56,12 @@ __global__ void __launch_bounds__(kWarps * 32)
         return;  // whole warp leaves together
     const int64_t qpos = pr.q_off + r;
     const int64_t head = (int64_t)bh * p.T;
-    const int64_t kv_off = pr.kv_off + (int64_t)sp * p.kv_split;
+    const int64_t kv_off = pr.kv_off + (int64_t)sp * p.kv_split;   // global position (mask)
+    const int64_t kv_row = pr.kv_row0 + (int64_t)sp * p.kv_split;  // row in the K/V tensors
     const int64_t kv_len = p.kv_split > 0 ? min(p.kv_split, p.kv_len - (int64_t)sp * p.kv_split) : p.kv_len;
     const float scale = 1.0f / sqrtf((float)D);
+    if (!RSA_DCHECK(pr.q_row0 + r < p.q_T, p.err, 0x41, pr.q_row0 + r))
+        return;
     const float *qrow = q + ((int64_t)bh * p.q_T + pr.q_row0 + r) * D;
 #pragma unroll
     for (int i = 0; i < PER; ++i)
@@ -77,8 +80,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     for (int64_t j0 = 0; j0 < kv_end; j0 += 32) {
         const int64_t j = j0 + lane;
         float s = -INFINITY;
-        if (j < kv_end) {
-            const float4 *kr = reinterpret_cast<const float4 *>(k + (head + kv_off + j) * D);
+        if (j < kv_end && RSA_DCHECK(kv_row + j < p.T, p.err, 0x42, kv_row + j)) {
+            const float4 *kr = reinterpret_cast<const float4 *>(k + (head + kv_row + j) * D);
             const float4 *qv = reinterpret_cast<const float4 *>(qs[warp]);
             float dot = 0.f;
 #pragma unroll 8
@@ -98,8 +101,10 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
         for (int i = 0; i < PER; ++i)
             o[i] *= alpha;
-        const int nk = (int)min((int64_t)32, kv_end - j0);
-        const float *vb = v + (head + kv_off + j0) * D;
+        int nk = (int)min((int64_t)32, kv_end - j0);
+        if (!RSA_DCHECK(kv_row + j0 + nk <= p.T, p.err, 0x43, kv_row + j0 + nk - 1))
+            nk = 0;
+        const float *vb = v + (head + kv_row + j0) * D;
         for (int kk = 0; kk < nk; ++kk) {
             const float pk = __shfl_sync(0xffffffffu, pj, kk);
 #pragma unroll
@@ -110,12 +115,16 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
 
     const int64_t orow = (int64_t)bh * pr.out_T + pr.out_t0 + r + (int64_t)sp * pr.split_stride;
+    if (!RSA_DCHECK(orow >= 0 && orow < pr.out_rows, p.err, 0x44, orow))
+        return;
     const bool empty = !(l > 0.f);
     const float lse_b = empty ? -INFINITY : m + logf(l);
     float wa = 0.f, wb = empty ? 0.f : 1.f / l, lse_out = lse_b;
+    bool use_acc = false;  // an accumulator row with lse = -inf is empty: not read
     if (pr.mode != kStore) {
         // fold into the running (acc, lse): M = max(a, b), L = M + ln(e^{a-M} + e^{b-M})
         const float a = pr.lse[orow];
+        use_acc = a > -INFINITY;
         const float M = fmaxf(a, lse_b);
         if (M > -INFINITY) {
             const float ea = expf(a - M), eb = expf(lse_b - M);
@@ -131,7 +140,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     const float *acc = pr.acc + orow * D;
 #pragma unroll
     for (int i = 0; i < PER; ++i)
-        out[lane + 32 * i] = pr.mode != kStore ? fmaf(o[i], wb, acc[lane + 32 * i] * wa) : o[i] * wb;
+        out[lane + 32 * i] = use_acc ? fmaf(o[i], wb, acc[lane + 32 * i] * wa) : o[i] * wb;
     __syncwarp();  // every lane has read lse[orow] before lane 0 replaces it
     if (lane == 0)
         pr.lse[orow] = lse_out;

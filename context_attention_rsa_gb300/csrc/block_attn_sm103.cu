@@ -105,7 +105,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pi = (int)(unit2 % p.npairs);
     const int bh = (int)(unit2 / p.npairs);
     const PairDesc &pr = p.pairs[pi];
-    const int64_t kv_off = pr.kv_off + (int64_t)sp * p.kv_split;
+    const int64_t kv_off = pr.kv_off + (int64_t)sp * p.kv_split;   // global position (mask)
+    const int64_t kv_row = pr.kv_row0 + (int64_t)sp * p.kv_split;  // row in the K/V tensors
     const int64_t kv_len = p.kv_split > 0 ? min(p.kv_split, p.kv_len - (int64_t)sp * p.kv_split) : p.kv_len;
     const int64_t q0 = (int64_t)qg * kBf16RowsPerCta;
     const int64_t rows_valid = min((int64_t)kBf16RowsPerCta, p.q_len - q0);
@@ -162,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     !ptx::mbar_wait(BAR(C::kKVE + slot), (use - 1) & 1, lim_ns, abort_flag, p.err, 1))
                     break;
                 const CUtensorMap *m = (ld & 1) ? &tm_v : &tm_k;
-                const int row = (int)(kv_off + (int64_t)(ld >> 1) * 128);
+                const int row = (int)(kv_row + (int64_t)(ld >> 1) * 128);
                 ptx::mbar_arrive_expect_tx(BAR(C::kKVF + slot), C::kTileBytes);
                 for (int b = 0; b < C::kBoxes; ++b)
                     ptx::tma_load_3d(sKV + slot * C::kTileBytes + b * C::kBoxBytes, m,

@@ -83,6 +83,11 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             vv[u] = ((int64_t)blockIdx.x * kUnroll + u) * kThreads + threadIdx.x;
+            if (vv[u] < nvec &&
+                !(RSA_DCHECK(mp.acc_t0 + (vv[u] >> log2_tpr) < p.T, p.err, 0x51, arow0 + (vv[u] >> log2_tpr)) &&
+                  RSA_DCHECK(brow0 + (vv[u] >> log2_tpr) < p.rows_per_pair, p.err, 0x52,
+                             brow0 + (vv[u] >> log2_tpr))))
+                vv[u] = nvec;  // out of range: skipped
             if (vv[u] < nvec) {
                 const int64_t r = vv[u] >> log2_tpr;
                 const int col = (int)(vv[u] & tpr_mask) * 8;
@@ -104,19 +109,25 @@ __global__ void __launch_bounds__(kThreads)
             const int64_t r = vv[u] >> log2_tpr;
             const int col = (int)(vv[u] & tpr_mask) * 8;
             const float M = fmaxf(a[u], b[u]);
-            float wa = 0.f, wb = 0.f, L = -INFINITY;
+            float L = -INFINITY;
             if (M > -INFINITY) {
                 const float ea = __expf(a[u] - M);
                 const float eb = __expf(b[u] - M);
                 const float sum = ea + eb;
                 const float inv = 1.f / sum;
                 L = M + __logf(sum);
-                wa = ea * inv;
-                wb = eb * inv;
-            }
+                const float wa = ea * inv, wb = eb * inv;
+                // A side with lse = -inf is empty: its o is not read (it may
+                // hold anything), rather than multiplied by a zero weight.
+                const bool ua = a[u] > -INFINITY, ub = b[u] > -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                x[u][i] = x[u][i] * wa + y[u][i] * wb;
+                for (int i = 0; i < 8; ++i)
+                    x[u][i] = (ua ? x[u][i] * wa : 0.f) + (ub ? y[u][i] * wb : 0.f);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    x[u][i] = 0.f;  // both sides empty: o = 0, lse = -inf
+            }
             const int64_t arow = arow0 + r;
             if (mp.final_) {
                 if (p.out_f32)

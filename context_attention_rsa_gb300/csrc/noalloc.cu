@@ -8,13 +8,15 @@
 // allowed or would stall a latency-critical stream.  For them this entry
 // point uses a fixed scratch array compiled into the library instead.
 //
-// The scratch is a file-scope __device__ array of kScratchBytes.  Once the
-// module holding it is loaded on a device (at the latest on this entry
-// point's first call there) that device keeps the memory until the process
-// exits.  In host code the array's name is only a host-side stand-in, so its
-// device address is looked up with cudaGetSymbolAddress once per device, with
-// that device current, on the first call made on it; make that first call
-// before any stream capture.
+// The scratch is a file-scope __device__ array of kScratchBytes.  It is
+// reserved on a device when the library's device code is loaded into that
+// device's context -- at the latest on this entry point's first call there,
+// and on every initialised device under eager module loading -- and stays
+// until the process exits.  In host code the array's name is only a host-side
+// stand-in, so its device address is looked up with cudaGetSymbolAddress on
+// the first call in each CUDA context (with that context current) and cached
+// under the context's unique id; make that first call before any stream
+// capture.
 //
 // Every call shares the one array and leaves its contents behind.  Nothing in
 // it needs to start at zero: the ring writes each accumulator row and each
@@ -22,7 +24,6 @@
 // streams, or different host threads without ordering between them) race on
 // the array and corrupt each other's results.
 #include <cstdio>
-#include <mutex>
 
 #include "rsa_internal.h"
 
@@ -31,30 +32,6 @@ namespace {
 constexpr size_t kScratchBytes = 64ull << 20;  // 64 MiB
 
 static __device__ __align__(256) unsigned char g_ring_scratch[kScratchBytes];
-
-constexpr int kMaxDevices = 64;
-
-rsa_status scratch_address(void **out)
-{
-    static std::mutex mu;
-    static void *cache[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return rsa::fail(RSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices)
-        return rsa::fail(RSA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
-    std::lock_guard<std::mutex> lock(mu);
-    if (!cache[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_ring_scratch);
-        if (e != cudaSuccess || p == nullptr)
-            return rsa::fail(RSA_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-        cache[dev] = p;
-    }
-    *out = cache[dev];
-    return RSA_OK;
-}
 
 }  // namespace
 
@@ -71,8 +48,10 @@ extern "C" rsa_status rsa_ring_attn_fwd_noalloc(const void *q, const void *k, co
                          "rsa_ring_attn_fwd_noalloc: this shape needs %zu bytes of scratch, the built-in "
                          "scratch holds %zu; use rsa_ring_attn_fwd with a caller workspace",
                          need, kScratchBytes);
+    // The array's name is only a host-side stand-in here; the kernels need its
+    // device address in the current context.
     void *scratch = nullptr;
-    st = scratch_address(&scratch);
+    st = rsa::symbol_address(reinterpret_cast<const void *>(g_ring_scratch), &scratch);
     if (st != RSA_OK)
         return st;
     return rsa_ring_attn_fwd(q, k, v, dt, B, H, T, d, N, causal, out, lse, scratch, kScratchBytes, stream);

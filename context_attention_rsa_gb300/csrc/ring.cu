@@ -24,6 +24,13 @@
 
 #include "rsa_internal.h"
 
+#define RSA_TRY(x)                     \
+    do {                               \
+        rsa_status st_ = (x);          \
+        if (st_ != RSA_OK)             \
+            return st_;                \
+    } while (0)
+
 namespace rsa {
 
 static thread_local char g_last_error[512] = "";
@@ -37,38 +44,132 @@ rsa_status fail(rsa_status st, const char *fmt, ...)
     return st;
 }
 
+namespace {
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+struct CtxFns {
+    CtxGetCurrentFn get_current = nullptr;
+    CtxGetIdFn get_id = nullptr;
+};
+
+// Driver calls reached through the runtime's entry-point query, so the
+// library does not link the driver library directly.
+const CtxFns &ctx_fns()
+{
+    static CtxFns f;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    return f;
+}
+
+// Unique id of the calling thread's current context; *have = false when no
+// context is current yet.
+rsa_status current_context_id(unsigned long long *id, bool *have)
+{
+    const CtxFns &f = ctx_fns();
+    if (!f.get_current || !f.get_id)
+        return fail(RSA_ERR_CUDA, "the CUDA driver lacks cuCtxGetCurrent/cuCtxGetId");
+    CUcontext ctx = nullptr;
+    if (f.get_current(&ctx) != CUDA_SUCCESS)
+        return fail(RSA_ERR_CUDA, "cuCtxGetCurrent failed");
+    *have = ctx != nullptr;
+    if (ctx && f.get_id(ctx, id) != CUDA_SUCCESS)
+        return fail(RSA_ERR_CUDA, "cuCtxGetId failed");
+    return RSA_OK;
+}
+
+}  // namespace
+
+rsa_status symbol_address(const void *symbol, void **out)
+{
+    struct Entry {
+        const void *sym;
+        unsigned long long ctx;
+        void *addr;
+    };
+    constexpr int kEntries = 128;
+    static Entry cache[kEntries] = {};
+    static int next = 0;
+    static std::mutex mu;
+    unsigned long long id = 0;
+    bool have = false;
+    rsa_status st = current_context_id(&id, &have);
+    if (st != RSA_OK)
+        return st;
+    if (have) {
+        std::lock_guard<std::mutex> lock(mu);
+        for (const Entry &e : cache)
+            if (e.sym == symbol && e.addr && e.ctx == id) {
+                *out = e.addr;
+                return RSA_OK;
+            }
+    }
+    // Not yet looked up in this context (this also creates the device's
+    // primary context when none is current).
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, symbol);
+    if (e != cudaSuccess || !p)
+        return fail(RSA_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    st = current_context_id(&id, &have);
+    if (st != RSA_OK)
+        return st;
+    if (!have)
+        return fail(RSA_ERR_CUDA, "no current CUDA context after the symbol lookup");
+    std::lock_guard<std::mutex> lock(mu);
+    cache[next] = Entry{symbol, id, p};
+    next = (next + 1) % kEntries;
+    *out = p;
+    return RSA_OK;
+}
+
 }  // namespace rsa
 
 using namespace rsa;
 
 namespace {
 
-__device__ unsigned int g_device_error;
+__device__ DeviceError g_device_error;
 
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_tc_kernel{0};
+
+// Host-side failure injection (off: -1).  When it reaches zero, the launch
+// wrapper reports a launch failure instead of launching, then disarms.
+std::atomic<int> g_inject_countdown{-1};
+
+// True if this launch is to fail (and the failure has been recorded).
+bool injected_failure(const char *what, rsa_status *st)
+{
+    int c = g_inject_countdown.load();
+    while (c >= 0) {
+        if (g_inject_countdown.compare_exchange_weak(c, c - 1)) {
+            if (c > 0)
+                return false;
+            *st = fail(RSA_ERR_CUDA, "%s: injected launch failure (rsa_debug_inject_launch_failure)", what);
+            return true;
+        }
+    }
+    return false;
+}
 
 constexpr int kMaxDevices = 64;
 
 rsa_status device_error_word(unsigned int **out)
 {
-    static std::mutex mu;
-    static unsigned int *cache[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return fail(RSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices)
-        return fail(RSA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
-    std::lock_guard<std::mutex> lock(mu);
-    if (!cache[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_device_error);
-        if (e != cudaSuccess)
-            return fail(RSA_ERR_CUDA, "cudaGetSymbolAddress(error word): %s", cudaGetErrorString(e));
-        cache[dev] = static_cast<unsigned int *>(p);
-    }
-    *out = cache[dev];
+    void *p = nullptr;
+    RSA_TRY(symbol_address(reinterpret_cast<const void *>(&g_device_error), &p));
+    *out = static_cast<unsigned int *>(p);
     return RSA_OK;
 }
 
@@ -124,13 +225,6 @@ rsa_status check_ptr(const void *p, const char *name)
         return fail(RSA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
     return RSA_OK;
 }
-
-#define RSA_TRY(x)                     \
-    do {                               \
-        rsa_status st_ = (x);          \
-        if (st_ != RSA_OK)             \
-            return st_;                \
-    } while (0)
 
 int round_pairs(int N, int causal, int r, int *qi, int *kj)
 {
@@ -206,6 +300,9 @@ rsa_status record(rsa_event_t ev, cudaStream_t s)
 rsa_status launch_block(const void *q, const void *k, const void *v, rsa_dtype dt, const BlockParams &p,
                         cudaStream_t s, Recorder *rec)
 {
+    rsa_status inj;
+    if (injected_failure("block attention launch", &inj))
+        return inj;
     if (rec)
         RSA_TRY(record(rec->start[rec->n], s));
     cudaError_t e = dt == RSA_BF16
@@ -223,6 +320,9 @@ rsa_status launch_block(const void *q, const void *k, const void *v, rsa_dtype d
 
 rsa_status launch_merge_rec(const MergeParams &p, cudaStream_t s, Recorder *rec)
 {
+    rsa_status inj;
+    if (injected_failure("merge launch", &inj))
+        return inj;
     if (rec)
         RSA_TRY(record(rec->start[rec->n], s));
     cudaError_t e = launch_merge(p, s);
@@ -304,10 +404,12 @@ rsa_status ring_run(const void *q, const void *k, const void *v, rsa_dtype dt, i
             pd.q_off = i * Tc;
             pd.q_row0 = pd.q_off;
             pd.kv_off = i * Tc;
+            pd.kv_row0 = pd.kv_off;
             pd.out = once ? out : static_cast<void *>(o_acc);
             pd.lse = lse;
             pd.out_T = T;
             pd.out_t0 = i * Tc;
+            pd.out_rows = BH * T;
             pd.out_f32 = once ? (dt == RSA_F32) : 1;
         }
         RSA_TRY(launch_block(q, k, v, dt, p, s, rec));
@@ -327,10 +429,12 @@ rsa_status ring_run(const void *q, const void *k, const void *v, rsa_dtype dt, i
                     pd.q_off = i * Tc;
                     pd.q_row0 = pd.q_off;
                     pd.kv_off = j * Tc;
+                    pd.kv_row0 = pd.kv_off;
                     pd.out = last ? out : static_cast<void *>(o_acc);
                     pd.lse = lse;
                     pd.out_T = T;
                     pd.out_t0 = i * Tc;
+                    pd.out_rows = BH * T;
                     pd.out_f32 = last ? (dt == RSA_F32) : 1;
                     pd.mode = last ? kMergeFinal : kMergeAcc;
                     pd.acc = o_acc;
@@ -354,6 +458,7 @@ rsa_status ring_run(const void *q, const void *k, const void *v, rsa_dtype dt, i
             m.lse_acc = lse;
             m.out = out;
             m.lse_out = lse;
+            m.err = err;
             for (int x = 0; x < gn; ++x) {
                 const int slot = g0 + x;
                 const int i = qi[slot], j = kj[slot];
@@ -363,10 +468,12 @@ rsa_status ring_run(const void *q, const void *k, const void *v, rsa_dtype dt, i
                 pd.q_off = i * Tc;
                 pd.q_row0 = pd.q_off;
                 pd.kv_off = j * Tc;
+                pd.kv_row0 = pd.kv_off;
                 pd.out = ob;
                 pd.lse = lb;
                 pd.out_T = Tc;
                 pd.out_t0 = 0;
+                pd.out_rows = BH * Tc;
                 pd.out_f32 = 1;
                 MergePair &mp = m.pairs[m.npairs++];
                 mp.acc_t0 = i * Tc;
@@ -477,6 +584,9 @@ rsa_status rsa_two_pass_attn_fwd(const void *q, const void *k, const void *v, rs
     float *S = static_cast<float *>(workspace);
     void *P = static_cast<char *>(workspace) + align256(rows * (size_t)T * 4);
     void *stats = static_cast<char *>(P) + align256(rows * (size_t)T * 2);
+    rsa_status inj;
+    if (injected_failure("two-pass launch", &inj))
+        return inj;
     cudaError_t e = launch_two_pass(q, k, v, (int64_t)B * H, T, N, causal, out, lse, S, P, stats,
                                     g_wait_limit_ns.load(), err, stream);
     if (e != cudaSuccess)
@@ -526,16 +636,21 @@ rsa_status rsa_decode_attn_fwd(const void *q, const void *k, const void *v, rsa_
             pd.q_off = T - q_len;
             pd.q_row0 = 0;
             pd.kv_off = i * Tc;
+            pd.kv_row0 = pd.kv_off;
             pd.out = part_o + (size_t)i * lay.sps * BH * q_len * d;
             pd.lse = part_lse + (size_t)i * lay.sps * BH * q_len;
             pd.out_T = q_len;
             pd.out_t0 = 0;
+            pd.out_rows = (int64_t)lay.sps * BH * q_len;
             pd.out_f32 = 1;
             pd.mode = kStore;
             pd.split_stride = BH * q_len;
         }
         RSA_TRY(launch_block(q, k, v, dt, p, stream, nullptr));
     }
+    rsa_status inj;
+    if (injected_failure("merge of decode splits", &inj))
+        return inj;
     cudaError_t e = launch_merge_splits(part_o, part_lse, lay.S, BH * q_len, d, out, dt == RSA_F32, lse, stream);
     if (e != cudaSuccess)
         return fail(RSA_ERR_CUDA, "merge of decode splits: %s", cudaGetErrorString(e));
@@ -563,11 +678,59 @@ rsa_status rsa_block_attn_fwd(const void *q, const void *k, const void *v, rsa_d
     pd.q_off = q_off;
     pd.q_row0 = pd.q_off;
     pd.kv_off = kv_off;
+    pd.kv_row0 = pd.kv_off;
     pd.out = o_blk;
     pd.lse = lse_blk;
     pd.out_T = q_len;
     pd.out_t0 = 0;
+    pd.out_rows = (int64_t)B * H * q_len;
     pd.out_f32 = dt == RSA_F32;
+    return launch_block(q, k, v, dt, p, stream, nullptr);
+}
+
+rsa_status rsa_block_attn_fold(const void *q, int64_t q_rows, const void *k, const void *v, int64_t kv_rows,
+                               rsa_dtype dt, int B, int H, int d, int64_t q_row0, int64_t q_pos, int64_t q_len,
+                               int64_t kv_row0, int64_t kv_pos, int64_t kv_len, int causal, int fold, float *acc,
+                               float *lse, void *out, rsa_stream_t stream)
+{
+    RSA_TRY(check_shape(dt, B, H, q_rows, d));
+    RSA_TRY(check_shape(dt, B, H, kv_rows, d));
+    RSA_TRY(check_ptr(q, "q"));
+    RSA_TRY(check_ptr(k, "k"));
+    RSA_TRY(check_ptr(v, "v"));
+    RSA_TRY(check_ptr(lse, "lse"));
+    if (fold < RSA_FOLD_FIRST || fold > RSA_FOLD_ONLY)
+        return fail(RSA_ERR_INVALID_ARG, "fold=%d is not one of RSA_FOLD_FIRST..RSA_FOLD_ONLY", fold);
+    if (fold != RSA_FOLD_ONLY)
+        RSA_TRY(check_ptr(acc, "acc"));
+    if (fold == RSA_FOLD_LAST || fold == RSA_FOLD_ONLY)
+        RSA_TRY(check_ptr(out, "out"));
+    if (q_len < 1 || kv_len < 1 || q_row0 < 0 || kv_row0 < 0 || q_row0 + q_len > q_rows ||
+        kv_row0 + kv_len > kv_rows || q_pos < 0 || kv_pos < 0)
+        return fail(RSA_ERR_INVALID_ARG,
+                    "pair rows [%lld, +%lld) of %lld query rows, [%lld, +%lld) of %lld key rows, positions "
+                    "%lld, %lld: outside the tensors or negative",
+                    (long long)q_row0, (long long)q_len, (long long)q_rows, (long long)kv_row0, (long long)kv_len,
+                    (long long)kv_rows, (long long)q_pos, (long long)kv_pos);
+    RSA_TRY(check_device_for(dt));
+    unsigned int *err = nullptr;
+    RSA_TRY(device_error_word(&err));
+    BlockParams p = base_params(dt, B, H, kv_rows, d, causal, q_len, kv_len, err);
+    p.q_T = q_rows;
+    PairDesc &pd = p.pairs[p.npairs++];
+    pd.q_off = q_pos;
+    pd.q_row0 = q_row0;
+    pd.kv_off = kv_pos;
+    pd.kv_row0 = kv_row0;
+    const bool to_out = fold == RSA_FOLD_LAST || fold == RSA_FOLD_ONLY;
+    pd.out = to_out ? out : static_cast<void *>(acc);
+    pd.lse = lse;
+    pd.out_T = q_rows;
+    pd.out_t0 = q_row0;
+    pd.out_rows = (int64_t)B * H * q_rows;
+    pd.out_f32 = to_out ? (dt == RSA_F32) : 1;
+    pd.mode = fold == RSA_FOLD_MERGE ? kMergeAcc : (fold == RSA_FOLD_LAST ? kMergeFinal : kStore);
+    pd.acc = acc;
     return launch_block(q, k, v, dt, p, stream, nullptr);
 }
 
@@ -602,6 +765,7 @@ static rsa_status merge_common(const float *o_acc, const float *lse_acc, const v
     m.lse_acc = const_cast<float *>(lse_acc);
     m.out = out;
     m.lse_out = lse_out;
+    RSA_TRY(device_error_word(&m.err));
     m.pairs[0].acc_t0 = 0;
     m.pairs[0].o_blk = o_blk;
     m.pairs[0].lse_blk = lse_blk;
@@ -727,6 +891,21 @@ rsa_status rsa_set_wait_limit_ns(uint64_t limit_ns)
     return RSA_OK;
 }
 
+int rsa_debug_checks(void)
+{
+#ifdef RSA_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+rsa_status rsa_debug_inject_launch_failure(int countdown)
+{
+    g_inject_countdown.store(countdown < 0 ? -1 : countdown);
+    return RSA_OK;
+}
+
 rsa_status rsa_set_block_kernel(int which)
 {
     if (which < RSA_BLOCK_KERNEL_AUTO || which > RSA_BLOCK_KERNEL_TWO_SM)
@@ -740,18 +919,22 @@ rsa_status rsa_check_device_error(rsa_stream_t stream)
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess)
         return fail(RSA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
-    unsigned int v = 0;
-    e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);
+    DeviceError rec{};
+    e = cudaMemcpyFromSymbol(&rec, g_device_error, sizeof rec);
     if (e != cudaSuccess)
         return fail(RSA_ERR_CUDA, "read error word: %s", cudaGetErrorString(e));
+    const unsigned int v = rec.word;
     if (v == 0)
         return RSA_OK;
-    const unsigned int zero = 0;
+    const DeviceError zero{};
     e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
     if (e != cudaSuccess)
         return fail(RSA_ERR_CUDA, "clear error word: %s", cudaGetErrorString(e));
     if (v & kDevErrTimeout)
         return fail(RSA_ERR_TIMEOUT, "a device wait exceeded its limit (site code 0x%02x)", v & 0xffu);
+    if (v & kDevErrBounds)
+        return fail(RSA_ERR_CUDA, "a device bounds check failed (site code 0x%02x, first bad index %lld)", v & 0xffu,
+                    (long long)rec.bad_index_plus1 - 1);
     return fail(RSA_ERR_CUDA, "device error word 0x%x", v);
 }
 

@@ -13,6 +13,32 @@ namespace rsa {
 
 // Device error word values (OR-ed with a site code in the low byte).
 constexpr unsigned int kDevErrTimeout = 0x100u;
+constexpr unsigned int kDevErrBounds = 0x200u;  // a bounds check of an RSA_DEBUG build failed
+
+// The device-side error record.  Kernels get a pointer to `word` and OR codes
+// into it; builds with RSA_DEBUG also keep the first out-of-range index (plus
+// one, so that 0 means none) of a failed bounds check.
+struct DeviceError {
+    unsigned int word;
+    unsigned int pad;
+    unsigned long long bad_index_plus1;
+};
+
+#ifdef RSA_DEBUG
+// Bounds check of an RSA_DEBUG build: false (and recorded, without a trap) if
+// `ok` is false; the caller then skips the access.
+__device__ __forceinline__ bool debug_check(bool ok, unsigned int *err, unsigned int site, long long idx)
+{
+    if (!ok && err) {
+        atomicOr(err, kDevErrBounds | site);
+        atomicCAS(&reinterpret_cast<DeviceError *>(err)->bad_index_plus1, 0ull, (unsigned long long)idx + 1ull);
+    }
+    return ok;
+}
+#define RSA_DCHECK(cond, err, site, idx) ::rsa::debug_check((cond), (err), (site), (long long)(idx))
+#else
+#define RSA_DCHECK(cond, err, site, idx) true
+#endif
 
 // Most pairs one kernel launch takes; longer pair lists are split.
 constexpr int kMaxPairsPerLaunch = 32;
@@ -31,7 +57,8 @@ enum EpilogueMode : int {
 struct PairDesc {
     int64_t q_off;   // global position of the first query row
     int64_t q_row0;  // row of the first query inside each head of the Q tensor
-    int64_t kv_off;  // global position of the first key
+    int64_t kv_off;  // global position of the first key (causal mask)
+    int64_t kv_row0; // row of the first key inside each head of the K/V tensors
     void *out;       // bf16 or fp32 (out_f32)
     float *lse;
     int64_t out_T;   // row pitch of out/lse per head
@@ -40,6 +67,7 @@ struct PairDesc {
     int mode;        // EpilogueMode
     const float *acc;  // fp32 accumulator (kMergeAcc: same as out; kMergeFinal: read only)
     int64_t split_stride;  // out/lse rows between consecutive key splits of this pair
+    int64_t out_rows;      // rows out, lse (and acc) hold from their base pointers (bounds checks)
 };
 
 struct BlockParams {
@@ -78,6 +106,7 @@ struct MergeParams {
     float *lse_acc;
     void *out;
     float *lse_out;
+    unsigned int *err;  // device error word (bounds checks of RSA_DEBUG builds)
     MergePair pairs[kMaxPairsPerLaunch];
 };
 
@@ -119,6 +148,13 @@ constexpr int kBf16RowsPerCluster = 512;
 bool block_attn_2sm_applies(const BlockParams &p);
 cudaError_t launch_block_attn_bf16_2sm(const void *q, const void *k, const void *v, const BlockParams &p,
                                        cudaStream_t s);
+
+// Device address of the __device__ variable at host-side stand-in `symbol`
+// in the calling thread's current CUDA context, looked up with
+// cudaGetSymbolAddress once per context.  The cache is keyed by the driver's
+// unique context id, so a context created later (after cudaDeviceReset, for
+// instance) gets a fresh lookup instead of a stale address.
+rsa_status symbol_address(const void *symbol, void **out);
 
 // Set the thread's last-error text and return `st`.
 rsa_status fail(rsa_status st, const char *fmt, ...);

@@ -195,8 +195,8 @@ __device__ __forceinline__ void softmax_warps(const SoftmaxCtx &c, const BlockPa
         const float lt = l[t] + xch[(t * 2 + (h ^ 1)) * 128 + row];
         const uint32_t tO = c.tmem + lane_addr + c.col_o[t];
         const int64_t rg = q0 + t * 128 + row;  // row inside the pair
-        const bool valid = rg < p.q_len;
         const int64_t orow = (int64_t)bh * pr.out_T + pr.out_t0 + rg + row_off;
+        const bool valid = rg < p.q_len && RSA_DCHECK(orow >= 0 && orow < pr.out_rows, p.err, 0x31, orow);
         // This pair's result is (O / l, lse_b).  A merging epilogue folds it
         // into the running (acc, lse) as the merge kernel does:
         // M = max(a, b), L = M + ln(e^{a-M} + e^{b-M}), o = acc e^{a-L} + o_b e^{b-L}.
@@ -206,8 +206,10 @@ __device__ __forceinline__ void softmax_warps(const SoftmaxCtx &c, const BlockPa
         float wb = empty ? 0.f : 1.f / lt;  // weight of the unnormalised O row
         float lse_out = lse_b;
         const bool merging = pr.mode != kStore;
+        bool use_acc = false;  // an accumulator row with lse = -inf is empty: not read
         if (merging && valid) {
             const float a = pr.lse[orow];
+            use_acc = a > -INFINITY;
             const float M = fmaxf(a, lse_b);
             if (M > -INFINITY) {
                 const float ea = ptx::ex2((a - M) * 1.4426950408889634f);
@@ -239,7 +241,7 @@ __device__ __forceinline__ void softmax_warps(const SoftmaxCtx &c, const BlockPa
             }
             if (valid) {
                 float v[32];
-                if (merging) {
+                if (use_acc) {
                     const float4 *src = reinterpret_cast<const float4 *>(pr.acc + orow * D + col);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {

@@ -84,12 +84,72 @@ rsa_status rsa_block_attn_fwd(const void *q, const void *k, const void *v, rsa_d
                               int causal, void *o_blk, float *lse_blk, rsa_stream_t stream);
 
 /*
+ * One (query block, KV block) pair on buffers that hold only part of the
+ * sequence, folded into a running fp32 accumulator -- the per-round step of
+ * a rank in a multi-GPU ring ([P1] "A better mental model: move blocks past
+ * the queries": a rank keeps its queries and receives other ranks' K/V
+ * blocks into a local buffer; [P1] "But softmax seems to require all
+ * attention scores at once": each block is folded into running statistics).
+ *   q        [B, H, q_rows, d]  this rank's queries (dtype dt)
+ *   k, v     [B, H, kv_rows, d] a K/V block (own or received), dtype dt
+ *   acc      [B, H, q_rows, d]  fp32 accumulator (normalised o)
+ *   lse      [B, H, q_rows]     fp32 running log-sum-exp (and the final lse)
+ *   out      [B, H, q_rows, d]  the result, dtype dt
+ * The pair is query rows [q_row0, q_row0 + q_len) -- at global sequence
+ * positions q_pos, q_pos + 1, ... -- against key rows [kv_row0, kv_row0 +
+ * kv_len) at global positions kv_pos, ...; the positions drive the causal
+ * mask (key position <= query position), the rows the memory accesses.
+ * fold says what happens to the pair's (o, lse) for those query rows:
+ *   RSA_FOLD_FIRST  written to acc and lse (the rows' first pair)
+ *   RSA_FOLD_MERGE  merged into acc and lse in place (the rule of rsa_merge)
+ *   RSA_FOLD_LAST   merged with acc and lse and written to out and lse
+ *                   (acc is only read)
+ *   RSA_FOLD_ONLY   the rows' only pair: written to out and lse (acc unused)
+ * A row whose running lse is -inf is empty and its acc values are not read.
+ * Requires the row ranges inside their tensors and non-negative positions;
+ * acc must be given unless fold is RSA_FOLD_ONLY, out for RSA_FOLD_LAST and
+ * RSA_FOLD_ONLY.
+ */
+enum { RSA_FOLD_FIRST = 0, RSA_FOLD_MERGE = 1, RSA_FOLD_LAST = 2, RSA_FOLD_ONLY = 3 };
+rsa_status rsa_block_attn_fold(const void *q, int64_t q_rows, const void *k, const void *v, int64_t kv_rows,
+                               rsa_dtype dt, int B, int H, int d,
+                               int64_t q_row0, int64_t q_pos, int64_t q_len,
+                               int64_t kv_row0, int64_t kv_pos, int64_t kv_len,
+                               int causal, int fold, float *acc, float *lse, void *out,
+                               rsa_stream_t stream);
+
+/*
+ * The pair list of one rank in a ring of N ranks over a sequence of T
+ * tokens ([P1] "A better mental model: move blocks past the queries": in
+ * round r rank i holds the K/V block of rank (i - r) mod N; [P1] "Causal
+ * attention gives us another optimization": pairs whose keys all lie after
+ * their queries are skipped).  Which tokens a rank owns:
+ *   RSA_LAYOUT_CONTIGUOUS  rank i owns tokens [i T/N, (i+1) T/N)
+ *   RSA_LAYOUT_ZIGZAG      with S = T/(2N): rank i owns the two pieces
+ *                          [i S, (i+1) S) and [(2N-1-i) S, (2N-i) S), in
+ *                          that order in its buffers, so that under the
+ *                          causal mask every rank does the same work in
+ *                          every round after the first
+ * Each step is 9 int64 values, in execution order (rounds ascending):
+ *   round, src_rank (= (rank - round) mod N, whose K/V block the step reads),
+ *   q_row0, q_pos, q_len, kv_row0, kv_pos, kv_len, fold
+ * ready for rsa_block_attn_fold (kv_row0 indexes src_rank's buffer).  Writes
+ * up to `cap` steps and their count to *n_steps.  Needs N | T (2N | T for
+ * zigzag).  Host only.
+ */
+enum { RSA_LAYOUT_CONTIGUOUS = 0, RSA_LAYOUT_ZIGZAG = 1 };
+rsa_status rsa_rank_ring_plan(int N, int rank, int64_t T, int causal, int layout, int64_t *steps, int cap,
+                              int *n_steps);
+
+/*
  * Online-softmax merge, in place, of [P1] "But softmax seems to require all
  * attention scores at once" written for normalised partials:
  *   a = lse_acc, b = lse_blk, M = max(a, b), L = M + ln(e^{a-M} + e^{b-M})
  *   o_acc <- o_acc e^{a-L} + o_blk e^{b-L},   lse_acc <- L
  * over `rows` contiguous rows of d values.  o_acc is fp32; o_blk has dtype
- * blk_dt.  Two empty rows (both lse = -inf) stay empty: o = 0, lse = -inf.
+ * blk_dt.  A row whose lse is -inf is empty: its o values are not used (they
+ * may hold anything, NaN included), so merging with it is the identity, and
+ * two empty rows give o = 0, lse = -inf.
  */
 rsa_status rsa_merge(float *o_acc, float *lse_acc, const void *o_blk, rsa_dtype blk_dt,
                      const float *lse_blk, int64_t rows, int d, rsa_stream_t stream);
@@ -140,11 +200,16 @@ rsa_status rsa_ring_attn_fwd(const void *q, const void *k, const void *v, rsa_dt
  * scratch array built into the library instead and allocates nothing.
  * Arguments and results are those of rsa_ring_attn_fwd; a shape whose
  * workspace (rsa_ring_attn_workspace_size) exceeds 64 MiB is rejected with
- * RSA_ERR_INVALID_ARG.  Once used on a device, the 64 MiB stay reserved there
- * until the process exits.  The first call on each device looks up the
- * scratch address; make it before any stream capture.  All calls share the
- * one scratch array, so calls that may overlap on the GPU (different streams
- * or unsynchronised host threads) race and must be serialised by the caller.
+ * RSA_ERR_INVALID_ARG.  The 64 MiB are reserved on a device when the
+ * library's device code is loaded into that device's context -- no later
+ * than this call's first use there, and, under eager module loading
+ * (CUDA_MODULE_LOADING=EAGER), on every device the process initialises even
+ * if this call is never made -- and stay reserved until the process exits.
+ * The first call in each CUDA context looks up the scratch address (and
+ * again in a new context, e.g. after cudaDeviceReset); make it before any
+ * stream capture.  All calls share the one scratch array, so calls that may
+ * overlap on the GPU (different streams or unsynchronised host threads) race
+ * and must be serialised by the caller.
  */
 rsa_status rsa_ring_attn_fwd_noalloc(const void *q, const void *k, const void *v, rsa_dtype dt,
                                      int B, int H, int64_t T, int d, int N, int causal,
@@ -192,6 +257,82 @@ rsa_status rsa_ring_attn_fwd_ex(const void *q, const void *k, const void *v, rsa
                                 void *out, float *lse, void *workspace, size_t ws_bytes,
                                 rsa_stream_t stream, rsa_event_t *ev_start, rsa_event_t *ev_stop,
                                 int *kind, int cap, int *n_launches);
+
+/*
+ * Page-locked host memory for streaming copies (the one call of this library
+ * that allocates; it allocates host memory only).  The block is `bytes`
+ * rounded up to the transparent-huge-page size, aligned to it, advised for
+ * huge pages, zeroed (so every page exists) and registered with the CUDA
+ * driver.  Rationale: copy-engine transfers from page-locked memory on base
+ * pages were measured to lose most of their bandwidth once the memory had sat
+ * idle for some seconds (from 211 GB/s towards 10-20 GB/s on GB300 hosts with
+ * 64 KiB pages), while huge-page-backed memory kept its speed.  Registering
+ * pins the pages, which may make the kernel migrate them and split huge
+ * pages; the huge-page share is therefore measured after registering, and a
+ * block below 90% is given back and allocated again (up to four attempts,
+ * the best one kept).  If no attempt reaches 90% the block comes from
+ * cudaHostAlloc instead.  *ptr receives the block (NULL on failure).
+ * Release it with rsa_host_free.  Host only; needs the CUDA driver.
+ */
+enum { RSA_HOST_HUGE = 1, RSA_HOST_PINNED = 2 };
+rsa_status rsa_host_alloc(size_t bytes, void **ptr);
+rsa_status rsa_host_free(void *ptr);
+/*
+ * What rsa_host_alloc handed out at `ptr`: its usable bytes, the bytes the
+ * kernel currently backs with huge pages (0 for RSA_HOST_PINNED), and its
+ * kind (RSA_HOST_HUGE: huge-page memory registered with the driver;
+ * RSA_HOST_PINNED: cudaHostAlloc).  Any output pointer may be NULL.
+ */
+rsa_status rsa_host_info(const void *ptr, size_t *bytes, size_t *huge_bytes, int *kind);
+
+/*
+ * The slab plan of rsa_ring_attn_fwd_host: how many heads each slab holds, in
+ * streaming order, for BH = B*H heads cut into about `groups` slabs of at most
+ * ceil(BH/groups) heads.  With ramp, the plan starts at an eighth of the
+ * largest slab and grows about 1.6x per slab, keeps equal slabs in the middle
+ * and shrinks back to an eighth at the end, so each slab's copy hides under
+ * the ring of the slab before it and only a small first copy in and last copy
+ * out are exposed.  Without ramp: equal slabs.  Writes up to `cap` entries
+ * and their count to *n_slabs.  Host only.
+ */
+rsa_status rsa_host_slab_plan(int BH, int groups, int ramp, int *slabs, int cap, int *n_slabs);
+
+/*
+ * Device workspace for rsa_ring_attn_fwd_host: two slots of the largest
+ * slab's q, k, v, out and lse, plus the ring workspace of one slab.
+ */
+rsa_status rsa_ring_attn_host_workspace_size(rsa_dtype dt, int B, int H, int64_t T, int d, int N,
+                                             int causal, size_t *bytes);
+
+/*
+ * rsa_ring_attn_fwd from host memory to host memory, the copies overlapped
+ * with the ring ([P1] "A better mental model: move blocks past the queries":
+ * blocks stream past queries that stay put).  q_host, k_host, v_host
+ * [B, H, T, d] (dtype dt) and out_host [B, H, T, d], lse_host [B, H, T] fp32
+ * are HOST pointers.  The B*H heads are independent problems, so they are cut
+ * into slabs (rsa_host_slab_plan(B*H, 8, 1)): while the ring of slab g runs on
+ * `stream`, slab g+1 is copied in and slab g-1 copied out on two copy streams
+ * the library creates for the current device on its first call there (with
+ * their events; all are kept until the process exits).  Device slabs are
+ * double-buffered in `workspace` (a DEVICE pointer, 256-byte aligned, at
+ * least rsa_ring_attn_host_workspace_size() bytes).  The results equal
+ * rsa_ring_attn_fwd's bit for bit.
+ *   - The host buffers should be page-locked (rsa_host_alloc, cudaHostAlloc or
+ *     cudaHostRegister); pageable memory works but the CUDA runtime then
+ *     stages each copy and the overlap is lost.
+ *   - The call returns once everything is enqueued; out_host and lse_host
+ *     hold the results once `stream` has passed the call.  The inputs must
+ *     not change, and the outputs must not be read, before then.
+ *   - Calls from several host threads on one device are serialised while
+ *     they enqueue.
+ *   - Argument errors are found before anything is enqueued.  A CUDA error
+ *     during enqueueing returns RSA_ERR_CUDA and may leave earlier slabs'
+ *     copies and rings enqueued.
+ */
+rsa_status rsa_ring_attn_fwd_host(const void *q_host, const void *k_host, const void *v_host,
+                                  rsa_dtype dt, int B, int H, int64_t T, int d, int N, int causal,
+                                  void *out_host, float *lse_host, void *workspace, size_t ws_bytes,
+                                  rsa_stream_t stream);
 
 /*
  * Decode against a distributed KV cache ([P1] "Training and inference stress
@@ -267,8 +408,33 @@ enum { RSA_BLOCK_KERNEL_AUTO = 0, RSA_BLOCK_KERNEL_ONE_SM = 1, RSA_BLOCK_KERNEL_
 rsa_status rsa_set_block_kernel(int which);
 
 /*
+ * Failure injection for testing callers' error handling (process wide, off
+ * by default).  With countdown = n >= 0, the library's next n kernel
+ * launches proceed and the one after that is not made: the call making it
+ * returns RSA_ERR_CUDA with "injected launch failure" in
+ * rsa_last_error_string(), exactly as if the launch had failed, and the
+ * injection switches itself off.  Launches of the same call before it have
+ * been enqueued; nothing after it is.  countdown < 0 switches it off.  Host
+ * only; no GPU fault is involved.
+ */
+rsa_status rsa_debug_inject_launch_failure(int countdown);
+
+/*
+ * 1 if this library was built with RSA_DEBUG: its kernels then check the
+ * indices of their computed global-memory accesses (output, accumulator and
+ * lse rows, fp32 K/V rows, merge rows); an access that fails its check is
+ * skipped, and the first failure's site code and index are recorded for
+ * rsa_check_device_error, which reports RSA_ERR_CUDA.  No trap.  0 for the
+ * normal build, whose kernels carry no such checks.  (The two-pass kernels
+ * are not covered.)
+ */
+int rsa_debug_checks(void);
+
+/*
  * Synchronise `stream`, then read and clear the device error word of the
- * current device: RSA_OK, or RSA_ERR_TIMEOUT if a kernel gave up on a wait.
+ * current device: RSA_OK, RSA_ERR_TIMEOUT if a kernel gave up on a wait, or
+ * RSA_ERR_CUDA if a bounds check of an RSA_DEBUG build failed (the text gives
+ * the site code and the first bad index).
  */
 rsa_status rsa_check_device_error(rsa_stream_t stream);
 

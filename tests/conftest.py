@@ -37,3 +37,17 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(autouse=True)
+def _debug_build_bounds_checks(request):
+    """Under RSA_DEBUG=1 (the library's bounds-checked build), every GPU test
+    ends by reading the device error word, so that a failed bounds check
+    anywhere in it fails the test."""
+    yield
+    if os.environ.get("RSA_DEBUG", "0") in ("", "0") or request.node.get_closest_marker("gpu") is None:
+        return
+    import torch
+    if torch.cuda.is_available():
+        import context_attention_rsa_gb300 as rsa
+        rsa.check_device_error()

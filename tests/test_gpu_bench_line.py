@@ -50,7 +50,11 @@ def test_gpu_arm_prints_one_full_contract_line():
     assert e["h2d_bytes_per_step"] == 3 * B * H * T * d * 2
     assert e["d2h_bytes_per_step"] == B * H * T * d * 2 + B * H * T * 4
     assert len(e["step_ms"]) == 2 and e["h2d_settle"]["probes_gbs"]
-    assert set(e["host_buffers"]) == {"q", "k", "v", "out", "lse"}
+    assert e["call"] == "rsa_ring_attn_fwd_host" and e["steps"] == 2
+    assert set(e["host_buffers"]) == {"q", "k", "v", "out+lse"}
+    for info in e["host_buffers"].values():
+        assert info["kind"] in ("registered-huge", "pinned") and info["bytes"] > 0
+    assert sum(e["slabs"]) == B * H
 
     assert line["gpu_launches"] > 0
     assert "sm_mhz" in line["clocks"] and "reasons" in line["clocks"]

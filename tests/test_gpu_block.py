@@ -74,15 +74,20 @@ def test_merge_matches_oracle(blk_dtype, d):
     o_blk[::11] = 0
     ref_o, ref_l = oracle.merge_lse(o_acc.double().numpy(), lse_acc.double().numpy(),
                                     o_blk.double().numpy(), lse_blk.double().numpy())
-    oa, la = o_acc.cuda(), lse_acc.cuda()
-    rsa.merge(oa, la, o_blk.cuda(), lse_blk.cuda())
+    # An empty row (lse = -inf) carries no values: the library must not read
+    # its o, so the GPU copies hold NaN there (the oracle's hold zeros).
+    o_acc_g, o_blk_g = o_acc.clone(), o_blk.clone()
+    o_acc_g[::7] = float("nan")
+    o_blk_g[::11] = float("nan")
+    oa, la = o_acc_g.cuda(), lse_acc.cuda()
+    rsa.merge(oa, la, o_blk_g.cuda(), lse_blk.cuda())
     torch.cuda.synchronize()
     assert_close(oa, la, ref_o, ref_l, torch.float32, what="merge")
     # finalising merge to bf16 leaves the accumulator alone
-    oa2, la2 = o_acc.cuda(), lse_acc.cuda()
-    out, lse_out = rsa.merge_finalize(oa2, la2, o_blk.cuda(), lse_blk.cuda(), out_dtype=torch.bfloat16)
+    oa2, la2 = o_acc_g.cuda(), lse_acc.cuda()
+    out, lse_out = rsa.merge_finalize(oa2, la2, o_blk_g.cuda(), lse_blk.cuda(), out_dtype=torch.bfloat16)
     torch.cuda.synchronize()
-    assert torch.equal(oa2.cpu(), o_acc) and torch.equal(la2.cpu(), lse_acc)
+    assert torch.equal(oa2.cpu().nan_to_num(7.0), o_acc_g.nan_to_num(7.0)) and torch.equal(la2.cpu(), lse_acc)
     assert_close(out, lse_out, ref_o, ref_l, torch.bfloat16, what="merge_finalize")
 
 
@@ -119,3 +124,60 @@ def test_block_outputs_leave_guard_bytes_alone():
     assert torch.all(l_buf[:pad] == 7) and torch.all(l_buf[pad + l.numel():] == 7)
     ro, rl = oracle.block(q, k, v, 367, q_len, 0, 700, True)
     assert_close(o, l, ro, rl, torch.bfloat16)
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.bfloat16, 64), (torch.float32, 64)])
+def test_fold_on_partial_buffers_matches_oracle(dtype, d):
+    # rsa_block_attn_fold: the query piece (positions 1024..1535) sits at row
+    # 256 of its own buffer and each K/V piece at row 88 of another, so rows
+    # and positions differ; FIRST, MERGE, LAST fold three pieces in an order
+    # that is not the positions' order.
+    need_cuda()
+    from context_attention_rsa_gb300 import rank_ring as rr
+    B, H, T = 1, 3, 1536
+    (q, k, v), _ = qkv_cuda(B, H, T, d, dtype, seed=61)
+    ro, rl = oracle.block(q, k, v, 1024, 512, 0, T, True)
+    qb = torch.full((B, H, 768, d), float("nan"), dtype=dtype)
+    qb[:, :, 256:768] = q[:, :, 1024:1536]
+    qb = qb.cuda()
+    acc = torch.full((B, H, 768, d), float("nan"), device="cuda")
+    lse = torch.full((B, H, 768), 7.0, device="cuda")
+    out = torch.full((B, H, 768, d), 3.0, dtype=dtype, device="cuda")
+    for kv_pos, fold in ((512, rr.FOLD_FIRST), (0, rr.FOLD_MERGE), (1024, rr.FOLD_LAST)):
+        kb = torch.zeros((B, H, 600, d), dtype=dtype)
+        vb = torch.zeros((B, H, 600, d), dtype=dtype)
+        kb[:, :, 88:600] = k[:, :, kv_pos:kv_pos + 512]
+        vb[:, :, 88:600] = v[:, :, kv_pos:kv_pos + 512]
+        step = dict(q_row0=256, q_pos=1024, q_len=512, kv_row0=88, kv_pos=kv_pos, kv_len=512, fold=fold)
+        rr.block_attn_fold(qb, kb.cuda(), vb.cuda(), step, True, acc, lse, out)
+        torch.cuda.synchronize()
+    rsa.check_device_error()
+    assert_close(out[:, :, 256:], lse[:, :, 256:], ro, rl, dtype, what="fold")
+    assert torch.all(out[:, :, :256] == 3.0) and torch.all(lse[:, :, :256] == 7.0)  # other rows untouched
+    # a single pair: RSA_FOLD_ONLY writes out and lse directly
+    ro2, rl2 = oracle.block(q, k, v, 1024, 512, 1024, 512, True)
+    kb = torch.zeros((B, H, 600, d), dtype=dtype)
+    vb = torch.zeros((B, H, 600, d), dtype=dtype)
+    kb[:, :, 88:600] = k[:, :, 1024:1536]
+    vb[:, :, 88:600] = v[:, :, 1024:1536]
+    out2 = torch.empty_like(out)
+    lse2 = torch.empty_like(lse)
+    step = dict(q_row0=256, q_pos=1024, q_len=512, kv_row0=88, kv_pos=1024, kv_len=512, fold=rr.FOLD_ONLY)
+    rr.block_attn_fold(qb, kb.cuda(), vb.cuda(), step, True, None, lse2, out2)
+    torch.cuda.synchronize()
+    assert_close(out2[:, :, 256:], lse2[:, :, 256:], ro2, rl2, dtype, what="fold only")
+
+
+def test_fold_rejects_bad_rows_and_modes():
+    need_cuda()
+    from context_attention_rsa_gb300 import rank_ring as rr
+    q = torch.zeros((1, 1, 256, 128), dtype=torch.bfloat16, device="cuda")
+    acc = torch.zeros((1, 1, 256, 128), device="cuda")
+    lse = torch.zeros((1, 1, 256), device="cuda")
+    good = dict(q_row0=0, q_pos=0, q_len=256, kv_row0=0, kv_pos=0, kv_len=256, fold=rr.FOLD_FIRST)
+    for bad in (dict(q_row0=1), dict(kv_len=257), dict(q_pos=-1), dict(fold=4)):
+        with pytest.raises(rsa.RsaError) as e:
+            rr.block_attn_fold(q, q, q, dict(good, **bad), True, acc, lse, q)
+        assert e.value.status == 1
+    with pytest.raises(rsa.RsaError):
+        rr.block_attn_fold(q, q, q, good, True, None, lse, q)  # FIRST needs the accumulator

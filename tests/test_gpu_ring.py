@@ -196,24 +196,27 @@ def test_fused_and_unfused_rings_agree_and_fused_launches_only_block_kernels():
     assert torch.equal(out[:, :, :T // N], o_a[:, :, :T // N])  # chunk 0 is never merged
 
 
-@pytest.mark.parametrize("B,H,T,groups,ramp", [(2, 5, 1024, 1, True), (2, 5, 1024, 3, True), (2, 5, 1024, 8, True),
-                                                (1, 64, 512, 8, True), (1, 64, 512, 8, False)])
-def test_ring_from_host_matches_device_ring(B, H, T, groups, ramp):
-    # The streamed host-to-host path (head slabs through three streams) gives
-    # exactly the device ring's result: every head is its own problem.  The
-    # 64-head cases run ramped slabs of 1 to 7 heads, and equal ones.
+@pytest.mark.parametrize("B,H,T,N,dtype", [(2, 5, 1024, 4, torch.bfloat16), (1, 64, 512, 4, torch.bfloat16),
+                                             (2, 37, 384, 3, torch.bfloat16), (1, 3, 256, 4, torch.float32)])
+def test_ring_from_host_matches_device_ring(B, H, T, N, dtype):
+    # rsa_ring_attn_fwd_host (head slabs streamed through the GPU, copies on
+    # the library's streams) gives exactly the device ring's result: every
+    # head is its own problem.  64 and 74 heads run ramped plans of slabs of
+    # 1 to 7 and 1 to 5 heads; torch-pinned inputs are accepted as well.
     need_cuda()
-    d, N = 128, 4
-    q, k, v = (t.pin_memory() for t in qkv_cuda(B, H, T, d, torch.bfloat16, seed=13)[0])
+    d = 64 if dtype == torch.float32 else 128
+    q, k, v = (t.pin_memory() for t in qkv_cuda(B, H, T, d, dtype, seed=13)[0])
     ref_o, ref_l = rsa.ring_attn(q.cuda(), k.cuda(), v.cuda(), N, True)
     bufs = {}
     for _ in range(2):  # second call reuses the buffers
-        oh, lh, bufs = rsa.ring_attn_from_host(q, k, v, N, True, buffers=bufs, groups=groups, ramp=ramp)
+        oh, lh, bufs = rsa.ring_attn_from_host(q, k, v, N, True, buffers=bufs)
         torch.cuda.synchronize()
         assert torch.equal(oh, ref_o.cpu()) and torch.equal(lh, ref_l.cpu())
+        oh.fill_(float("nan"))
+        lh.fill_(float("nan"))
 
 
-def test_host_empty_is_page_locked_and_streams_bit_exactly():
+def test_host_empty_is_page_locked_huge_and_streams_bit_exactly():
     need_cuda()
     B, H, T, d, N = 1, 64, 512, 128, 4
     (q, k, v), _ = qkv_cuda(B, H, T, d, torch.bfloat16, seed=21)
@@ -221,23 +224,44 @@ def test_host_empty_is_page_locked_and_streams_bit_exactly():
     for th, t in ((qh, q), (kh, k), (vh, v)):
         th.copy_(t)
         assert th.is_pinned() and torch.equal(th, t)
+        info = rsa.host_info(th)
+        assert info["bytes"] >= t.numel() * 2 and info["kind"] in ("registered-huge", "pinned")
+        if info["kind"] == "registered-huge":  # rsa_host_alloc kept it only if >= 90% of it is huge
+            assert info["huge_bytes"] >= info["bytes"] * 9 // 10
+        assert rsa.host_kind(th) == info["kind"]
     ref_o, ref_l = rsa.ring_attn(q.cuda(), k.cuda(), v.cuda(), N, True)
     bufs = {}
     oh, lh, bufs = rsa.ring_attn_from_host(qh, kh, vh, N, True, buffers=bufs)
     torch.cuda.synchronize()
-    assert bufs["out_host"].is_pinned() and bufs["lse_host"].is_pinned()
+    assert oh.is_pinned() and lh.is_pinned()
     assert torch.equal(oh, ref_o.cpu()) and torch.equal(lh, ref_l.cpu())
-    for th in (qh, kh, vh):
-        # a block on huge pages is registered by host_empty and unregistered by
-        # host_free; otherwise it came from torch's pinned allocator
-        kind = rsa.host_kind(th)
-        assert kind in ("registered-huge", "pinned")
-        registered = th.untyped_storage().data_ptr() in rsa._host_blocks
-        assert registered == (kind == "registered-huge")
-        rsa.host_free(th)
-        assert th.is_pinned() != registered
     assert rsa.host_kind(q) == "pageable"
-    rsa.host_free(q)  # not made by host_empty: left alone
+    # a block goes back to the system with its last tensor
+    addr = qh.untyped_storage().data_ptr()
+    del qh
+    import gc
+    gc.collect()
+    assert addr not in rsa._host_blocks
+
+
+def test_ring_from_host_waits_for_the_callers_stream():
+    # The copies start only after work already enqueued on the caller's
+    # stream: inputs written there just before the call are the ones used.
+    need_cuda()
+    B, H, T, d, N = 1, 16, 1024, 128, 4
+    (q, k, v), (qd, kd, vd) = qkv_cuda(B, H, T, d, torch.bfloat16, seed=41)
+    qh, kh, vh = (rsa.host_empty(t.shape, t.dtype) for t in (q, k, v))
+    for th in (qh, kh, vh):
+        th.zero_()
+    ref_o, ref_l = rsa.ring_attn(qd, kd, vd, N, True)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(50_000_000)  # keep the stream busy, then write the inputs on it
+        for th, td in ((qh, qd), (kh, kd), (vh, vd)):
+            th.copy_(td, non_blocking=True)
+        oh, lh, _ = rsa.ring_attn_from_host(qh, kh, vh, N, True, stream=s)
+    s.synchronize()
+    assert torch.equal(oh, ref_o.cpu()) and torch.equal(lh, ref_l.cpu())
 
 
 @pytest.mark.parametrize("fused", [False, True], ids=["merge_kernel", "fused_merge"])

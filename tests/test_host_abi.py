@@ -187,3 +187,38 @@ def test_slab_plan_covers_every_head_and_ramps_gently(BH, groups):
     for a, b in zip(plan, plan[1:]):
         assert b <= max(a + 1, (a * 8) // 5 + 1), plan
     assert rsa.slab_plan(BH, groups, ramp=False) == [cap] * (BH // cap) + ([BH % cap] if BH % cap else [])
+
+
+def test_host_streaming_workspace_and_validation():
+    lib = rsa.load()
+    n = ctypes.c_size_t(0)
+    # page-1 shape: 512 heads, largest slab 57 heads (ramped plan of 8 groups)
+    assert lib.rsa_ring_attn_host_workspace_size(1, 8, 64, 32768, 128, 4, 1, ctypes.byref(n)) == 0
+    hg = max(rsa.slab_plan(512, 8))
+    slab = hg * 32768 * 128 * 2
+    ring = rsa.workspace_size(__import__("torch").bfloat16, 1, hg, 32768, 128, 4, True)
+    assert n.value == 2 * (4 * slab + hg * 32768 * 4) + (ring + 255) // 256 * 256
+    assert lib.rsa_ring_attn_host_workspace_size(1, 1, 1, 100, 128, 3, 1, ctypes.byref(n)) == 1  # N does not divide T
+    args = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, lse=FAKE, ws=0x100000, nb=1 << 40)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return lib.rsa_ring_attn_fwd_host(a["q"], a["k"], a["v"], 1, 1, 4, 1024, 128, 4, 1, a["out"], a["lse"],
+                                          a["ws"], a["nb"], None)
+    assert call(q=None) == 1 and b"NULL" in lib.rsa_last_error_string()
+    assert call(lse=None) == 1
+    assert call(ws=0x100010) == 1 and b"256-byte" in lib.rsa_last_error_string()
+    assert call(nb=1024) == 1 and b"needed" in lib.rsa_last_error_string()
+
+
+def test_host_alloc_rejects_bad_arguments():
+    lib = rsa.load()
+    p = ctypes.c_void_p(0)
+    assert lib.rsa_host_alloc(0, ctypes.byref(p)) == 1 and not p.value
+    assert lib.rsa_host_alloc(16, None) == 1
+    assert lib.rsa_host_free(FAKE) == 1 and b"rsa_host_alloc" in lib.rsa_last_error_string()
+    assert lib.rsa_host_info(FAKE, None, None, None) == 1
+    slabs = (ctypes.c_int * 4)()
+    cnt = ctypes.c_int(0)
+    assert lib.rsa_host_slab_plan(512, 8, 1, slabs, 4, ctypes.byref(cnt)) == 1 and cnt.value == 14
+    assert lib.rsa_host_slab_plan(0, 8, 1, slabs, 4, ctypes.byref(cnt)) == 1
