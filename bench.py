@@ -240,7 +240,8 @@ def main():
     ap.add_argument("--workload", default="page1_causal_bf16")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-fused", action="store_true", help="skip timing the fused-merge ring variant")
+    ap.add_argument("--no-separate-merge", action="store_true",
+                    help="skip timing the ring variant with the separate merge kernel")
     ap.add_argument("--no-decode", action="store_true", help="skip timing decode on the million-token cache")
     ap.add_argument("--no-two-pass", action="store_true", help="skip timing the two-pass RSA form")
     ap.add_argument("--no-other-workloads", action="store_true",
@@ -324,45 +325,69 @@ def main():
     torch.cuda.synchronize()
     rsa.check_device_error()
 
+    # the default ring folds every pair in the block epilogue: all its launches are block launches
     blk_ms = sum(ev0[s][i].elapsed_time(ev1[s][i]) for s in range(args.steps) for i in range(n_launch)
                  if kinds[i] == 0) / args.steps
-    mrg_ms = sum(ev0[s][i].elapsed_time(ev1[s][i]) for s in range(args.steps) for i in range(n_launch)
-                 if kinds[i] == 1) / args.steps
     n_blk = sum(1 for x in kinds if x == 0)
-    n_mrg = sum(1 for x in kinds if x == 1)
 
     flops = useful_flops(B, H, T, d, causal)
     value = whole_job_tflops(flops, world, ms_step)
     peaks = read_peaks()
     blk_tflops = flops / (blk_ms * 1e-3) / 1e12
     mbytes = merge_bytes_per_step(w, lambda r: rsa.ring_schedule(N, causal, r))
-    mrg_gbs = mbytes / (mrg_ms * 1e-3) / 1e9 if mrg_ms > 0 else None
+    # Per round (one block launch per round when a round has at most 32
+    # pairs): time, useful FLOPs and pair-equivalents (a full Tc x Tc block is
+    # one; a causal diagonal block (Tc+1)/(2 Tc)).
+    rounds = None
+    if n_launch == N:
+        Tc = T // N
+        rounds = []
+        for r in range(N):
+            pe = sum(((Tc + 1) / (2 * Tc)) if (causal and i == j) else 1.0 for (i, j) in rsa.ring_schedule(N, causal, r))
+            r_ms = sum(ev0[s][r].elapsed_time(ev1[s][r]) for s in range(args.steps)) / args.steps
+            r_fl = 4.0 * B * H * d * Tc * Tc * pe
+            rounds.append({"round": r, "ms": r_ms, "pair_equivalents": pe, "ms_per_pair_equivalent": r_ms / pe,
+                           "tflops": r_fl / (r_ms * 1e-3) / 1e12})
 
-    # ---- the fused-merge ring (each pair's epilogue folds into the accumulator)
-    f1 = None
-    if not args.no_fused:
-        ws_f = torch.empty(max(rsa.workspace_size(q.dtype, B, H, T, d, N, causal, fused=True), 1),
+    # ---- the ring with the separate merge kernel (RSA_RING_SEPARATE_MERGE) ------
+    # Each round's partials go to the workspace and one merge launch folds
+    # them in: the merge kernel's HBM roofline is measured here.
+    sep = None
+    mrg_ms = mrg_gbs = None
+    n_mrg = 0
+    if not args.no_separate_merge:
+        ws_s = torch.empty(max(rsa.workspace_size(q.dtype, B, H, T, d, N, causal, fused=False), 1),
                            dtype=torch.uint8, device=dev)
-        n_f = rsa.ring_launch_count(N, causal, fused=True)
+        n_s = rsa.ring_launch_count(N, causal, fused=False)
         for _ in range(max(args.warmup, 0)):
-            rsa.ring_attn(q, k, v, N, causal, out=out, lse=lse, workspace=ws_f, fused=True)
-        fe0 = [[torch.cuda.Event(enable_timing=True) for _ in range(n_f)] for _ in range(args.steps)]
-        fe1 = [[torch.cuda.Event(enable_timing=True) for _ in range(n_f)] for _ in range(args.steps)]
+            rsa.ring_attn(q, k, v, N, causal, out=out, lse=lse, workspace=ws_s, fused=False)
         barrier()
         torch.cuda.synchronize()
         t_start.record(stream)
         for s_ in range(args.steps):
-            rsa.ring_attn_timed(q, k, v, N, causal, out, lse, ws_f, fe0[s_], fe1[s_], fused=True)
+            rsa.ring_attn(q, k, v, N, causal, out=out, lse=lse, workspace=ws_s, fused=False)
         t_stop.record(stream)
         torch.cuda.synchronize()
         barrier()
         rsa.check_device_error()
-        f_ms = max_over_ranks(pg, t_start.elapsed_time(t_stop), dev) / args.steps
-        f_blk = sum(fe0[s_][i].elapsed_time(fe1[s_][i]) for s_ in range(args.steps) for i in range(n_f)) / args.steps
-        f1 = {"value": whole_job_tflops(flops, world, f_ms), "unit": UNIT, "ms_per_step": f_ms,
-              "block_kernel_tflops": flops / (f_blk * 1e-3) / 1e12, "launches_per_step": n_f,
-              "workspace_bytes": int(ws_f.numel())}
-        del ws_f
+        s_ms = max_over_ranks(pg, t_start.elapsed_time(t_stop), dev) / args.steps
+        se0 = [[torch.cuda.Event(enable_timing=True) for _ in range(n_s)] for _ in range(args.steps)]
+        se1 = [[torch.cuda.Event(enable_timing=True) for _ in range(n_s)] for _ in range(args.steps)]
+        s_kinds = None
+        for s_ in range(args.steps):
+            s_kinds = rsa.ring_attn_timed(q, k, v, N, causal, out, lse, ws_s, se0[s_], se1[s_], fused=False)
+        torch.cuda.synchronize()
+        rsa.check_device_error()
+        s_blk = sum(se0[s_][i].elapsed_time(se1[s_][i]) for s_ in range(args.steps) for i in range(n_s)
+                    if s_kinds[i] == 0) / args.steps
+        mrg_ms = sum(se0[s_][i].elapsed_time(se1[s_][i]) for s_ in range(args.steps) for i in range(n_s)
+                     if s_kinds[i] == 1) / args.steps
+        n_mrg = sum(1 for x in s_kinds if x == 1)
+        mrg_gbs = mbytes / (mrg_ms * 1e-3) / 1e9 if mrg_ms > 0 else None
+        sep = {"value": whole_job_tflops(flops, world, s_ms), "unit": UNIT, "ms_per_step": s_ms,
+               "block_kernel_tflops": flops / (s_blk * 1e-3) / 1e12, "block_kernel_ms_per_step": s_blk,
+               "merge_ms_per_step": mrg_ms, "launches_per_step": n_s, "workspace_bytes": int(ws_s.numel())}
+        del ws_s
 
     # ---- decode against a sharded million-token KV cache (HBM-bound) ---------
     dec = None
@@ -564,13 +589,14 @@ def main():
                          "unit": "TFLOP/s", "frac": blk_tflops / peaks["bf16_tflops_sustained"],
                          "traffic": block_traffic() if w.name == "page1_causal_bf16" else None,
                          "kernel": "block_attn_bf16_kernel<128>",
-                         "launches_per_step": n_blk, "ms_per_step": blk_ms,
+                         "launches_per_step": n_blk, "ms_per_step": blk_ms, "rounds": rounds,
                          "peak_source": peaks["source"] + " bf16_tflops_sustained"},
             "merge": {"bound": "hbm", "achieved": mrg_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                       "frac": (mrg_gbs / peaks["hbm_gbs"]) if mrg_gbs else None,
                       "algorithmic_bytes_per_step": mbytes, "launches_per_step": n_mrg, "ms_per_step": mrg_ms,
+                      "measured_in": "separate_merge_ring",
                       "peak_source": peaks["source"] + " hbm_gbs"},
-            "fused_merge_ring": f1,
+            "separate_merge_ring": sep,
             "decode": dec,
             "two_pass_rsa": tp,
             "e2e": e2e,

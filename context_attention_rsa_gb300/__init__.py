@@ -180,17 +180,21 @@ def _check_qkv(q, k, v) -> Tuple[int, int, int, int]:
 
 
 RSA_RING_FUSED_MERGE = 1
+RSA_RING_SEPARATE_MERGE = 2
+
+
+def _ring_flags(fused: bool) -> int:
+    return RSA_RING_FUSED_MERGE if fused else RSA_RING_SEPARATE_MERGE
 
 
 def workspace_size(dtype: torch.dtype, B: int, H: int, T: int, d: int, N: int, causal: bool,
-                   fused: bool = False) -> int:
+                   fused: bool = True) -> int:
+    """Workspace bytes of the ring: the fused merge (default) or, with
+    fused=False, the separate merge kernel (RSA_RING_SEPARATE_MERGE)."""
     n = ctypes.c_size_t(0)
     dt = RSA_F32 if dtype == torch.float32 else RSA_BF16
-    if fused:
-        _call("rsa_ring_attn_workspace_size_ex", dt, B, H, T, d, N, int(bool(causal)), RSA_RING_FUSED_MERGE,
-              ctypes.byref(n))
-    else:
-        _call("rsa_ring_attn_workspace_size", dt, B, H, T, d, N, int(bool(causal)), ctypes.byref(n))
+    _call("rsa_ring_attn_workspace_size_ex", dt, B, H, T, d, N, int(bool(causal)), _ring_flags(fused),
+          ctypes.byref(n))
     return int(n.value)
 
 
@@ -253,10 +257,11 @@ def merge_finalize(o_acc, lse_acc, o_blk, lse_blk, out_dtype=torch.bfloat16, out
 
 
 def ring_attn(q, k, v, N: int, causal: bool, out=None, lse=None, workspace=None,
-              stream=None, fused: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
+              stream=None, fused: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
     """The whole ring: (out [B, H, T, d] in q's dtype, lse [B, H, T] fp32).
-    fused=True folds each pair into the accumulator in the block epilogue
-    (RSA_RING_FUSED_MERGE) instead of launching the merge kernel."""
+    By default (rsa_ring_attn_fwd) each pair's block epilogue folds it into
+    the accumulator; fused=False computes partials and launches the merge
+    kernel instead (RSA_RING_SEPARATE_MERGE)."""
     B, H, T, d = _check_qkv(q, k, v)
     if out is None:
         out = torch.empty_like(q)
@@ -266,13 +271,13 @@ def ring_attn(q, k, v, N: int, causal: bool, out=None, lse=None, workspace=None,
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     if fused:
-        _call("rsa_ring_attn_fwd_ex", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
-              int(bool(causal)), RSA_RING_FUSED_MERGE, out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
-              workspace.numel() * workspace.element_size(), _stream(stream), None, None, None, 0, None)
-    else:
         _call("rsa_ring_attn_fwd", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
               int(bool(causal)), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
               workspace.numel() * workspace.element_size(), _stream(stream))
+    else:
+        _call("rsa_ring_attn_fwd_ex", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
+              int(bool(causal)), RSA_RING_SEPARATE_MERGE, out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+              workspace.numel() * workspace.element_size(), _stream(stream), None, None, None, 0, None)
     return out, lse
 
 
@@ -293,7 +298,7 @@ def ring_attn_noalloc(q, k, v, N: int, causal: bool, out=None, lse=None,
 
 
 def ring_attn_timed(q, k, v, N: int, causal: bool, out, lse, workspace, events_start: Sequence,
-                    events_stop: Sequence, stream=None, fused: bool = False) -> List[int]:
+                    events_stop: Sequence, stream=None, fused: bool = True) -> List[int]:
     """ring_attn that records the given torch.cuda.Event pairs around each
     kernel launch; returns the launch kinds (0 block attention, 1 merge)."""
     B, H, T, d = _check_qkv(q, k, v)
@@ -307,19 +312,19 @@ def ring_attn_timed(q, k, v, N: int, causal: bool, out, lse, workspace, events_s
     kinds = (ctypes.c_int * cap)()
     n = ctypes.c_int(0)
     if fused:
-        _call("rsa_ring_attn_fwd_ex", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
-              int(bool(causal)), RSA_RING_FUSED_MERGE, out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+        _call("rsa_ring_attn_fwd_timed", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
+              int(bool(causal)), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
               workspace.numel() * workspace.element_size(), _stream(stream), ev_s, ev_e, kinds, cap,
               ctypes.byref(n))
     else:
-        _call("rsa_ring_attn_fwd_timed", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
-              int(bool(causal)), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+        _call("rsa_ring_attn_fwd_ex", q.data_ptr(), k.data_ptr(), v.data_ptr(), _dt(q), B, H, T, d, N,
+              int(bool(causal)), RSA_RING_SEPARATE_MERGE, out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
               workspace.numel() * workspace.element_size(), _stream(stream), ev_s, ev_e, kinds, cap,
               ctypes.byref(n))
     return [kinds[i] for i in range(n.value)]
 
 
-def ring_launch_count(N: int, causal: bool, fused: bool = False) -> int:
+def ring_launch_count(N: int, causal: bool, fused: bool = True) -> int:
     """Kernel launches one ring makes (block-attention plus merge launches)."""
     n = 0
     for r in range(N):

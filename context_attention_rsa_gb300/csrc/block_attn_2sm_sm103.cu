@@ -310,7 +310,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ctx.xch = reinterpret_cast<float *>(gbase + C::kXchOff);
         ctx.abort_flag = abort_flag;
         ctx.lim_ns = lim_ns;
-        softmax_warps<D>(ctx, p, pr, q0, n, kv_off, kv_len, bh, 0, [&](int t) {
+        softmax_warps<D, 2>(ctx, p, pr, q0, n, n, kv_off, kv_len, bh, 0, [&](int t) {
             __syncwarp();
             if (lane == 0)
                 ptx::mbar_arrive_remote(BAR0(C::kPF + t));

@@ -30,6 +30,7 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
+#include <cstring>
 #include <mutex>
 
 #include "ptx_sm103.cuh"
@@ -42,11 +43,19 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 
 template <int D>
 struct Cfg {
+    // Threads per query row in the softmax (8 softmax warps), then one TMA
+    // warp and one MMA warp.  Four threads per row (16 softmax warps) was
+    // measured slower: more exchange and TMEM instructions per tile.
+    static constexpr int kTPR = 2;
+    static constexpr int kSoftmaxWarps = 4 * kTPR;
+    static constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+    static constexpr int kProducerWarp = kSoftmaxWarps;
+    static constexpr int kMmaWarp = kSoftmaxWarps + 1;
+    static constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
     static constexpr int kBoxes = D / 64;            // 128-byte-wide TMA boxes per tile
     static constexpr uint32_t kBoxBytes = 128u * 128u; // 128 rows x 128 bytes
     static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
@@ -54,8 +63,8 @@ struct Cfg {
     static constexpr uint32_t kQOff = 0;
     static constexpr uint32_t kKVOff = 2 * kTileBytes;
     static constexpr uint32_t kBarOff = kKVOff + kStages * kTileBytes;
-    static constexpr uint32_t kXchOff = kBarOff + 256;  // [2 tiles][2 halves][128 rows] floats
-    static constexpr uint32_t kSmemBytes = kXchOff + 2048 + 1024;
+    static constexpr uint32_t kXchOff = kBarOff + 256;  // [2 tiles][kTPR parts][128 rows] floats
+    static constexpr uint32_t kSmemBytes = kXchOff + 2 * kTPR * 128 * 4 + 1024;
     static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
     // barrier indices
     static constexpr int kQF = 0;
@@ -65,15 +74,25 @@ struct Cfg {
     static constexpr int kPF = kSF + 2;
     static constexpr int kOF = kPF + 2;
     static constexpr int kDrain = kOF + 2;
-    static constexpr int kNumBars = kDrain + 1;
+    static constexpr int kQFree = kDrain + 1;   // every MMA but the last step's PVs has completed
+    static constexpr int kAccFull = kQFree + 1; // the staged accumulator rows have landed
+    static constexpr int kNumBars = kAccFull + 1;
+    // Merging epilogues stage the CTA's fp32 accumulator rows in shared memory:
+    // tile 0 over Q, tile 1 over two K/V slots, in 32-column boxes of 128 rows
+    // (128-byte swizzle).
+    static constexpr int kAccBoxes = D / 32;
+    static constexpr uint32_t kAccBoxBytes = 128u * 32u * 4u;
+    static_assert(kAccBoxes * kAccBoxBytes == 2 * kTileBytes, "an accumulator tile fills two K/V slots");
+    static_assert(kStages % 2 == 0, "two consecutive slots never wrap");
     static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
     block_attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
+                           const __grid_constant__ CUtensorMap tm_acc,
                            const __grid_constant__ BlockParams p)
 {
     using C = Cfg<D>;
@@ -114,6 +133,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.causal)
         kv_end = min(kv_end, pr.q_off + q0 + rows_valid - kv_off);
     const int n = kv_end > 0 ? (int)((kv_end + 127) / 128) : 0;
+    // Tile 0 (the CTA's first 128 rows) may need one key tile fewer: under the
+    // causal mask a key tile that starts after its last row is all masked
+    // (the last step of every CTA on a diagonal pair), so tile 0 skips it.
+    int n0 = n;
+    if (p.causal && n > 0) {
+        const int64_t e0 = min(kv_len, pr.q_off + q0 + min((int64_t)128, rows_valid) - kv_off);
+        n0 = e0 > 0 ? (int)((e0 + 127) / 128) : 0;
+    }
+    // The fold into the accumulator reads its rows from shared memory, staged
+    // by TMA while the last step runs.
+    const bool stage_acc = p.acc_staged && pr.mode != kStore && n > 0;
+    const uint32_t acc_stage[2] = {sQ, sKV + (uint32_t)((2 * n) % C::kStages) * C::kTileBytes};
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(BAR(C::kQF), 1);
@@ -123,21 +154,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(BAR(C::kSF + t), 1);
-            ptx::mbar_init(BAR(C::kPF + t), 256);
+            ptx::mbar_init(BAR(C::kPF + t), C::kSoftmaxThreads);
             ptx::mbar_init(BAR(C::kOF + t), 1);
         }
         ptx::mbar_init(BAR(C::kDrain), 1);
+        ptx::mbar_init(BAR(C::kQFree), 1);
+        ptx::mbar_init(BAR(C::kAccFull), 1);
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
-    if (warp == 9) {
+    if (warp == C::kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
         ptx::tmem_relinquish();
     }
-    if (warp == 8 && lane == 0) {
+    if (warp == C::kProducerWarp && lane == 0) {
         ptx::tma_prefetch_desc(&tm_q);
         ptx::tma_prefetch_desc(&tm_k);
         ptx::tma_prefetch_desc(&tm_v);
+        if (p.acc_staged)
+            ptx::tma_prefetch_desc(&tm_acc);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -145,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const uint64_t lim_ns = p.wait_limit_ns;
 
-    if (warp == 8) {
+    if (warp == C::kProducerWarp) {
         // =========================== TMA producer ===========================
         if (lane == 0 && n > 0) {
             int last_use[C::kStages];
@@ -156,6 +191,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int b = 0; b < C::kBoxes; ++b)
                     ptx::tma_load_3d(sQ + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, BAR(C::kQF),
                                      b * 64, (int)(pr.q_row0 + q0 + t * 128), bh);
+            // The accumulator rows a merging epilogue will stage: into L2 now,
+            // so that their load at the end of the main loop is an L2 hit.
+            if (stage_acc)
+                for (int t = 0; t < 2; ++t)
+                    for (int b = 0; b < C::kAccBoxes; ++b)
+                        ptx::tma_prefetch_l2_3d(&tm_acc, b * 32, (int)(pr.out_t0 + q0 + t * 128), bh);
             for (int ld = 0; ld < 2 * n; ++ld) {
                 const int slot = ld % C::kStages;
                 const int use = ld / C::kStages;
@@ -170,14 +211,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      BAR(C::kKVF + slot), b * 64, row, bh);
                 last_use[slot] = use;
             }
+            // Accumulator rows of a merging epilogue: once every MMA but the
+            // last PVs has completed, Q and every slot but V(n-1)'s are free.
+            bool acc_issued = false;
+            if (stage_acc && ptx::mbar_wait(BAR(C::kQFree), 0, lim_ns, abort_flag, p.err, 4)) {
+                ptx::mbar_arrive_expect_tx(BAR(C::kAccFull), 2 * C::kAccBoxes * C::kAccBoxBytes);
+                for (int t = 0; t < 2; ++t)
+                    for (int b = 0; b < C::kAccBoxes; ++b)
+                        ptx::tma_load_3d(acc_stage[t] + b * C::kAccBoxBytes, &tm_acc, BAR(C::kAccFull), b * 32,
+                                         (int)(pr.out_t0 + q0 + t * 128), bh);
+                acc_issued = true;
+            }
             // Let every copy this thread started land before the CTA can exit.
             volatile int no_abort = 0;
             ptx::mbar_wait(BAR(C::kQF), 0, lim_ns, &no_abort, p.err, 2);
             for (int s = 0; s < C::kStages; ++s)
                 if (last_use[s] >= 0)
                     ptx::mbar_wait(BAR(C::kKVF + s), last_use[s] & 1, lim_ns, &no_abort, p.err, 3);
+            if (acc_issued)
+                ptx::mbar_wait(BAR(C::kAccFull), 0, lim_ns, &no_abort, p.err, 5);
         }
-    } else if (warp == 9) {
+    } else if (warp == C::kMmaWarp) {
         // ============================ MMA issuer ============================
         if (lane == 0 && n > 0) {
             const uint32_t idesc_qk = ptx::idesc_bf16_f32(128, 128, false);
@@ -219,11 +273,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok)
                 ok = ptx::mbar_wait(BAR(C::kKVF + 0), 0, lim_ns, abort_flag, p.err, 11);
             if (ok) {
-                issue_qk(0, 0);
-                ptx::mma_commit(BAR(C::kSF + 0));
+                if (n0 > 0) {
+                    issue_qk(0, 0);
+                    ptx::mma_commit(BAR(C::kSF + 0));
+                } else {
+                    ptx::mma_commit(BAR(C::kOF + 0));  // tile 0 sees no key at all
+                }
                 issue_qk(1, 0);
                 ptx::mma_commit(BAR(C::kSF + 1));
                 ptx::mma_commit(BAR(C::kKVE + 0));
+                if (n == 1)
+                    ptx::mma_commit(BAR(C::kQFree));  // that was the last S MMA
             }
             for (int j = 0; ok && j < n; ++j) {
                 const int vld = 2 * j + 1;
@@ -232,21 +292,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok)
                     break;
                 // tile 0
-                ok = pv_tile(0, vslot, j);
-                if (!ok)
-                    break;
                 const bool more = j + 1 < n;
-                if (more) {
-                    const int kld = 2 * (j + 1);
-                    kslot = kld % C::kStages;
-                    ok = ptx::mbar_wait(BAR(C::kKVF + kslot), (kld / C::kStages) & 1, lim_ns, abort_flag,
-                                        p.err, 14);
+                if (j < n0) {
+                    ok = pv_tile(0, vslot, j);
                     if (!ok)
                         break;
-                    issue_qk(0, kslot);
-                    ptx::mma_commit(BAR(C::kSF + 0));
-                } else {
-                    ptx::mma_commit(BAR(C::kOF + 0));
+                    if (j + 1 < n0) {
+                        const int kld = 2 * (j + 1);
+                        kslot = kld % C::kStages;
+                        ok = ptx::mbar_wait(BAR(C::kKVF + kslot), (kld / C::kStages) & 1, lim_ns, abort_flag,
+                                            p.err, 14);
+                        if (!ok)
+                            break;
+                        issue_qk(0, kslot);
+                        ptx::mma_commit(BAR(C::kSF + 0));
+                    } else {
+                        ptx::mma_commit(BAR(C::kOF + 0));
+                    }
                 }
                 // tile 1
                 ok = pv_tile(1, vslot, j);
@@ -254,9 +316,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 ptx::mma_commit(BAR(C::kKVE + vslot));
                 if (more) {
+                    if (j + 1 >= n0) {  // tile 0 did not wait for K(j+1)
+                        const int kld = 2 * (j + 1);
+                        kslot = kld % C::kStages;
+                        ok = ptx::mbar_wait(BAR(C::kKVF + kslot), (kld / C::kStages) & 1, lim_ns, abort_flag,
+                                            p.err, 14);
+                        if (!ok)
+                            break;
+                    }
                     issue_qk(1, kslot);
                     ptx::mma_commit(BAR(C::kSF + 1));
                     ptx::mma_commit(BAR(C::kKVE + kslot));
+                    if (j + 2 == n)
+                        ptx::mma_commit(BAR(C::kQFree));  // that was the last S MMA
                 } else {
                     ptx::mma_commit(BAR(C::kOF + 1));
                 }
@@ -280,16 +352,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             ctx.bar_of[t] = BAR(C::kOF + t);
         }
         ctx.xch = reinterpret_cast<float *>(gbase + C::kXchOff);
+        ctx.acc_staged = stage_acc;
+        ctx.acc_smem[0] = acc_stage[0];
+        ctx.acc_smem[1] = acc_stage[1];
+        ctx.acc_box_bytes = C::kAccBoxBytes;
+        ctx.bar_acc = BAR(C::kAccFull);
         ctx.abort_flag = abort_flag;
         ctx.lim_ns = lim_ns;
-        softmax_warps<D>(ctx, p, pr, q0, n, kv_off, kv_len, bh, (int64_t)sp * pr.split_stride,
+        softmax_warps<D, C::kTPR>(ctx, p, pr, q0, n, n0, kv_off, kv_len, bh, (int64_t)sp * pr.split_stride,
                          [&](int t) { ptx::mbar_arrive(BAR(C::kPF + t)); });
     }
 
     // ---- teardown --------------------------------------------------------------
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == C::kMmaWarp) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
     }
@@ -304,13 +381,43 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t BH, int64_t T, int d)
     return make_bf16_map_sw128(m, ptr, 3, dims, strides, box);
 }
 
-template <int D>
-cudaError_t launch_d(const void *q, const void *k, const void *v, const BlockParams &p, cudaStream_t s)
+// [B*H, out_T, d] fp32 accumulator view with 128-row x 32-column boxes and
+// 128-byte swizzle.
+bool make_acc_map(CUtensorMap *m, const float *acc, int64_t BH, int64_t out_T, int d)
 {
-    const int64_t BH = (int64_t)p.B * p.H;
-    CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, q, BH, p.q_T, D) || !make_map(&mk, k, BH, p.T, D) || !make_map(&mv, v, BH, p.T, D))
+    const uint64_t dims[3] = {(uint64_t)d, (uint64_t)out_T, (uint64_t)BH};
+    const uint64_t strides[2] = {(uint64_t)d * 4, (uint64_t)out_T * d * 4};
+    const uint32_t box[3] = {32, 128, 1};
+    return make_f32_map_sw128(m, acc, 3, dims, strides, box);
+}
+
+template <int D>
+cudaError_t launch_d(const void *q, const void *k, const void *v, const BlockParams &p_in, cudaStream_t s)
+{
+    const int64_t BH = (int64_t)p_in.B * p_in.H;
+    CUtensorMap mq, mk, mv, macc;
+    if (!make_map(&mq, q, BH, p_in.q_T, D) || !make_map(&mk, k, BH, p_in.T, D) || !make_map(&mv, v, BH, p_in.T, D))
         return cudaErrorInvalidValue;
+    // Merging pairs stage their accumulator rows by TMA when they all fold into
+    // one accumulator of one row pitch, unsplit (else the epilogue reads them
+    // from global memory).
+    BlockParams p = p_in;
+    const PairDesc *first = nullptr;
+    bool same = true;
+    for (int i = 0; i < p.npairs; ++i) {
+        const PairDesc &pr = p.pairs[i];
+        if (pr.mode == kStore)
+            continue;
+        if (!first)
+            first = &pr;
+        else if (pr.acc != first->acc || pr.out_T != first->out_T)
+            same = false;
+        if (pr.split_stride != 0 || (reinterpret_cast<uintptr_t>(pr.acc) & 15u))
+            same = false;
+    }
+    p.acc_staged = first && same && p.n_split == 1 && make_acc_map(&macc, first->acc, BH, first->out_T, D) ? 1 : 0;
+    if (!p.acc_staged)
+        memset(&macc, 0, sizeof macc);
     const int64_t grid = (int64_t)p.n_qgroups * p.npairs * BH * p.n_split;
     if (grid <= 0)
         return cudaSuccess;
@@ -321,7 +428,7 @@ cudaError_t launch_d(const void *q, const void *k, const void *v, const BlockPar
                                          (int)smem);
     if (e != cudaSuccess)
         return e;
-    block_attn_bf16_kernel<D><<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, p);
+    block_attn_bf16_kernel<D><<<(unsigned)grid, Cfg<D>::kThreads, smem, s>>>(mq, mk, mv, macc, p);
     return cudaGetLastError();
 }
 

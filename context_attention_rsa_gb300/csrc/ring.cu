@@ -794,7 +794,7 @@ rsa_status rsa_ring_attn_workspace_size(rsa_dtype dt, int B, int H, int64_t T, i
     RSA_TRY(check_shape(dt, B, H, T, d));
     if (N < 1 || N > T || T % N != 0)
         return fail(RSA_ERR_INVALID_ARG, "N=%d must be >= 1 and divide T=%lld", N, (long long)T);
-    *bytes = ws_layout(dt, B, H, T, d, N, causal, false).total;
+    *bytes = ws_layout(dt, B, H, T, d, N, causal, true).total;
     return RSA_OK;
 }
 
@@ -803,8 +803,22 @@ rsa_status rsa_ring_attn_fwd(const void *q, const void *k, const void *v, rsa_dt
                              rsa_stream_t stream)
 {
     WsLayout lay;
-    RSA_TRY(validate_ring(q, k, v, dt, B, H, T, d, N, out, lse, workspace, ws_bytes, causal, false, &lay));
-    return ring_run(q, k, v, dt, B, H, T, d, N, causal, out, lse, workspace, lay, false, stream, nullptr);
+    RSA_TRY(validate_ring(q, k, v, dt, B, H, T, d, N, out, lse, workspace, ws_bytes, causal, true, &lay));
+    return ring_run(q, k, v, dt, B, H, T, d, N, causal, out, lse, workspace, lay, true, stream, nullptr);
+}
+
+// Which merge a ring variant uses: the fold in the block epilogue (the
+// default, RSA_RING_FUSED_MERGE) or partials and the merge kernel
+// (RSA_RING_SEPARATE_MERGE).
+static rsa_status ring_flags(unsigned flags, bool *fused)
+{
+    const unsigned known = RSA_RING_FUSED_MERGE | RSA_RING_SEPARATE_MERGE;
+    if (flags & ~known)
+        return fail(RSA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    if ((flags & RSA_RING_FUSED_MERGE) && (flags & RSA_RING_SEPARATE_MERGE))
+        return fail(RSA_ERR_INVALID_ARG, "RSA_RING_FUSED_MERGE and RSA_RING_SEPARATE_MERGE exclude each other");
+    *fused = (flags & RSA_RING_SEPARATE_MERGE) == 0;
+    return RSA_OK;
 }
 
 static rsa_status ring_profiled(const void *q, const void *k, const void *v, rsa_dtype dt, int B, int H,
@@ -812,9 +826,8 @@ static rsa_status ring_profiled(const void *q, const void *k, const void *v, rsa
                                 void *workspace, size_t ws_bytes, rsa_stream_t stream, rsa_event_t *ev_start,
                                 rsa_event_t *ev_stop, int *kind, int cap, int *n_launches)
 {
-    if (flags & ~(unsigned)RSA_RING_FUSED_MERGE)
-        return fail(RSA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
-    const bool fused = (flags & RSA_RING_FUSED_MERGE) != 0;
+    bool fused = true;
+    RSA_TRY(ring_flags(flags, &fused));
     WsLayout lay;
     RSA_TRY(validate_ring(q, k, v, dt, B, H, T, d, N, out, lse, workspace, ws_bytes, causal, fused, &lay));
     const bool timed = ev_start || ev_stop || kind;
@@ -853,12 +866,12 @@ rsa_status rsa_ring_attn_workspace_size_ex(rsa_dtype dt, int B, int H, int64_t T
 {
     if (!bytes)
         return fail(RSA_ERR_INVALID_ARG, "bytes is NULL");
-    if (flags & ~(unsigned)RSA_RING_FUSED_MERGE)
-        return fail(RSA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    bool fused = true;
+    RSA_TRY(ring_flags(flags, &fused));
     RSA_TRY(check_shape(dt, B, H, T, d));
     if (N < 1 || N > T || T % N != 0)
         return fail(RSA_ERR_INVALID_ARG, "N=%d must be >= 1 and divide T=%lld", N, (long long)T);
-    *bytes = ws_layout(dt, B, H, T, d, N, causal, (flags & RSA_RING_FUSED_MERGE) != 0).total;
+    *bytes = ws_layout(dt, B, H, T, d, N, causal, fused).total;
     return RSA_OK;
 }
 

@@ -83,6 +83,7 @@ struct BlockParams {
     int n_qgroups;          // query-row groups per pair (rows per CTA granularity)
     uint64_t wait_limit_ns;
     int tc_kernel;          // tensor-core kernel choice: 0 automatic (one-SM), 1 one-SM, 2 two-SM where it applies
+    int acc_staged;         // set by the one-SM launcher: merging epilogues read the accumulator staged by TMA
     unsigned int *err;      // device error word
     PairDesc pairs[kMaxPairsPerLaunch];
 };

@@ -1,5 +1,5 @@
 // Register-level helpers shared by the tensor-core kernels: bit casts, bf16
-// packing, three-input max and the named barrier of the 256 softmax threads of
+// packing, three-input max and the named barrier of the softmax threads of
 // the block-attention kernels (one-SM and two-SM).
 #pragma once
 
@@ -26,26 +26,36 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
     return r;
 }
 
-// Named barrier 1 over the 256 softmax threads (warps 0-7).
+// Named barrier 1 over the NT softmax threads (the first NT / 32 warps).
+template <int NT = 256>
 __device__ __forceinline__ void softmax_bar_sync()
 {
-    asm volatile("barrier.cta.sync 1, 256;" ::: "memory");
+    asm volatile("barrier.cta.sync 1, %0;" ::"n"(NT) : "memory");
 }
 
 // The same barrier, returning whether `v` holds in every softmax thread, so
 // that a decision to give up is taken by all of them together.
+template <int NT = 256>
 __device__ __forceinline__ bool softmax_bar_and(bool v)
 {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred pi, po;\n\t"
         "setp.ne.u32 pi, %1, 0;\n\t"
-        "barrier.cta.red.and.pred po, 1, 256, pi;\n\t"
+        "barrier.cta.red.and.pred po, 1, %2, pi;\n\t"
         "selp.u32 %0, 1, 0, po;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)v)
+        : "r"((uint32_t)v), "n"(NT)
         : "memory");
     return r != 0;
+}
+
+// 16-byte shared-memory load (a staged row piece).
+__device__ __forceinline__ float4 ld_shared_v4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
 }
 
 }  // namespace tc

@@ -49,72 +49,112 @@ struct SoftmaxCtx {
     float *xch;           // shared scratch: [2 tiles][2 halves][128 rows] floats
     volatile int *abort_flag;
     uint64_t lim_ns;
+    // A merging epilogue with staged accumulator rows: tile t's rows are at
+    // acc_smem[t] as 32-column boxes of 128 rows x 128 bytes (128-byte
+    // swizzle), acc_box_bytes apart, complete once bar_acc's phase 0 is.
+    bool acc_staged = false;
+    uint32_t acc_smem[2] = {0u, 0u};
+    uint32_t acc_box_bytes = 0;
+    uint32_t bar_acc = 0;
 };
 
-// Rows [q0, q0 + 256) of pair `pr` (two tiles of 128), keys [kv_off,
-// kv_off + kv_len) in n steps of 128.  Output row r of the pair goes to row
-// bh * out_T + out_t0 + r + row_off.  Every one of the 256 softmax threads
-// calls this; all leave it together.
-template <int D, class Arrive>
-__device__ __forceinline__ void softmax_warps(const SoftmaxCtx &c, const BlockParams &p, const PairDesc &pr,
-                                              int64_t q0, int n, int64_t kv_off, int64_t kv_len, int bh,
-                                              int64_t row_off, Arrive arrive)
+// A load issued where it stands (the value is needed much later).
+__device__ __forceinline__ float ld_global_early(const float *p)
 {
+    float v;
+    asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+// Rows [q0, q0 + 256) of pair `pr` (two tiles of 128), keys [kv_off,
+// kv_off + kv_len) in n steps of 128; tile 0 takes only the first n0 <= n of
+// them (the MMA issuer computes no S, P or PV of tile 0 after those).  Output row r of the pair goes to row
+// bh * out_T + out_t0 + r + row_off.  TPR threads share each query row (TPR =
+// 2 or 4): the first 128 * TPR threads of the CTA call this, and all leave it
+// together.  Thread (warp w, lane) reads TMEM lane 32 (w mod 4) + lane and takes
+// part h = w / 4 of every step: keys [h K, h K + K) with K = 128 / TPR, and
+// output columns [h D / TPR, (h + 1) D / TPR).
+template <int D, int TPR, class Arrive>
+__device__ __forceinline__ void softmax_warps(const SoftmaxCtx &c, const BlockParams &p, const PairDesc &pr,
+                                              int64_t q0, int n, int n0, int64_t kv_off, int64_t kv_len,
+                                              int bh, int64_t row_off, Arrive arrive)
+{
+    static_assert(TPR == 2 || TPR == 4, "two or four threads per query row");
+    constexpr int NT = 128 * TPR;     // softmax threads
+    constexpr int K = 128 / TPR;      // keys of a step per thread
+    constexpr int OC = D / TPR;       // output columns per thread
+    static_assert(OC % 32 == 0, "output columns come in 32-column TMEM loads");
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int h = warp >> 2;
     const int wi = warp & 3;
     const int row = wi * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(wi * 32) << 16;
-    float *xch = c.xch;
+    float *xch = c.xch;  // [2 tiles][TPR parts][128 rows]
     const float sl2 = 1.4426950408889634f / sqrtf((float)D);  // log2(e) / sqrt(d)
     float m_used[2] = {-INFINITY, -INFINITY};                   // kept maxima, log2 units
-    float l[2] = {0.f, 0.f};                                    // this half's row sums
+    float l[2] = {0.f, 0.f};                                    // this part's row sums
     int64_t allowed[2];  // keys [0, allowed) of the key range visible to the row, per tile
+    float lse_run[2] = {-INFINITY, -INFINITY};  // the running lse a merging epilogue folds into
     for (int t = 0; t < 2; ++t) {
         const int64_t qpos = pr.q_off + q0 + t * 128 + row;
         allowed[t] = p.causal ? min(kv_len, qpos - kv_off + 1) : kv_len;
+        // Only this CTA writes its rows' running lse, and only in the epilogue:
+        // load it now so that its latency hides under the main loop.
+        const int64_t rg = q0 + t * 128 + row;
+        const int64_t orow = (int64_t)bh * pr.out_T + pr.out_t0 + rg + row_off;
+        if (pr.mode != kStore && rg < p.q_len && RSA_DCHECK(orow >= 0 && orow < pr.out_rows, p.err, 0x32, orow))
+            lse_run[t] = ld_global_early(pr.lse + orow);
     }
     bool ok = true;
     for (int j = 0; ok && j < n; ++j) {
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
+            if (t == 0 && j >= n0)
+                continue;  // the same for every softmax thread
             const uint32_t tS = c.tmem + lane_addr + c.col_s[t];
             const uint32_t tO = c.tmem + lane_addr + c.col_o[t];
             bool got = ptx::mbar_wait(c.bar_sf[t], j & 1, c.lim_ns, c.abort_flag, p.err, 20);
             got = __all_sync(0xffffffffu, got);
-            uint32_t s[64];
+            uint32_t s[K];
             float mx = -INFINITY;
             if (got) {
                 ptx::tc_fence_after();
-                ptx::tmem_ld64(tS + 64 * h, s);
-                ptx::tmem_ld_wait64(s);
-                const int64_t lim = allowed[t] - (int64_t)j * 128 - 64 * h;
-                if (lim < 64) {
+                if constexpr (K == 64) {
+                    ptx::tmem_ld64(tS + K * h, s);
+                    ptx::tmem_ld_wait64(s);
+                } else {
+                    ptx::tmem_ld32(tS + K * h, s);
+                    ptx::tmem_ld_wait(s);
+                }
+                const int64_t lim = allowed[t] - (int64_t)j * 128 - K * h;
+                if (lim < K) {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i)
+                    for (int i = 0; i < K; ++i)
                         if ((int64_t)i >= lim)
                             s[i] = f2u(-INFINITY);
                 }
-                // row max of this half: four independent chains of three-input max
+                // row max of this part: four independent chains of three-input max
                 float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int i = 0; i < 64; i += 8) {
+                for (int i = 0; i < K; i += 8) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         m4[k] = fmax3(m4[k], u2f(s[i + 2 * k]), u2f(s[i + 2 * k + 1]));
                 }
                 mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
-                xch[(t * 2 + h) * 128 + row] = mx;
+                xch[(t * TPR + h) * 128 + row] = mx;
             }
             // Every S load of this tile is done (and every softmax thread knows
-            // whether every wait succeeded) before any half writes P over S.
+            // whether every wait succeeded) before any part writes P over S.
             ptx::tc_fence_before();
-            ok = softmax_bar_and(got);
+            ok = softmax_bar_and<NT>(got);
             ptx::tc_fence_after();
             if (!ok)
                 break;
-            mx = fmaxf(mx, xch[(t * 2 + (h ^ 1)) * 128 + row]);
+#pragma unroll
+            for (int o = 1; o < TPR; ++o)
+                mx = fmaxf(mx, xch[(t * TPR + ((h + o) % TPR)) * 128 + row]);
             const float mnew = mx * sl2;
             const bool need =
                 (mnew > -INFINITY) && (m_used[t] == -INFINITY || mnew > m_used[t] + kRescaleThreshold);
@@ -129,9 +169,9 @@ __device__ __forceinline__ void softmax_warps(const SoftmaxCtx &c, const BlockPa
                     // the commit that signalled S_t(j) also covered PV_t(j-1): O_t is stable
                     const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
-                    for (int k = 0; k < D / 64; ++k) {
+                    for (int k = 0; k < OC / 32; ++k) {
                         uint32_t o[32];
-                        const uint32_t ta = tO + h * (D / 2) + k * 32;
+                        const uint32_t ta = tO + h * OC + k * 32;
                         ptx::tmem_ld32(ta, o);
                         ptx::tmem_ld_wait(o);
 #pragma unroll
@@ -145,26 +185,25 @@ __device__ __forceinline__ void softmax_warps(const SoftmaxCtx &c, const BlockPa
                 }
             }
             // p = 2^(s * log2(e)/sqrt(d) - m) as bf16 pairs over S: keys
-            // [64h + 32q, 64h + 32q + 32) go to packed columns [32h + 16q, +16).
+            // [K h, K h + K) go to packed columns [K h / 2, K h / 2 + K / 2).
             const float neg = (m_used[t] == -INFINITY) ? 0.f : -m_used[t];
             const float2 c2 = make_float2(sl2, sl2);
             const float2 n2 = make_float2(neg, neg);
             float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                              make_float2(0.f, 0.f)};
-            uint32_t pk[32];
+            uint32_t pk[K / 2];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int e = 32 * q + 2 * i;
-                    const float2 x = __ffma2_rn(make_float2(u2f(s[e]), u2f(s[e + 1])), c2, n2);
-                    const float p0 = ptx::ex2(x.x);
-                    const float p1 = ptx::ex2(x.y);
-                    acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
-                    pk[16 * q + i] = pack_bf16(p0, p1);
-                }
+            for (int i = 0; i < K / 2; ++i) {
+                const float2 x = __ffma2_rn(make_float2(u2f(s[2 * i]), u2f(s[2 * i + 1])), c2, n2);
+                const float p0 = ptx::ex2(x.x);
+                const float p1 = ptx::ex2(x.y);
+                acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(p0, p1));
+                pk[i] = pack_bf16(p0, p1);
             }
-            ptx::tmem_st32(tS + 32 * h, pk);
+            if constexpr (K == 64)
+                ptx::tmem_st32(tS + (K / 2) * h, pk);
+            else
+                ptx::tmem_st16(tS + (K / 2) * h, pk);
             // P and the rescaled O complete before the MMA may read them
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
@@ -181,18 +220,25 @@ __device__ __forceinline__ void softmax_warps(const SoftmaxCtx &c, const BlockPa
         fin = ptx::mbar_wait(c.bar_of[t], 0, c.lim_ns, c.abort_flag, p.err, 21);
         fin = __all_sync(0xffffffffu, fin);
     }
-    softmax_bar_sync();  // the exchange slots are free again
-    if (ok) {
-        xch[(0 * 2 + h) * 128 + row] = l[0];
-        xch[(1 * 2 + h) * 128 + row] = l[1];
+    if (c.acc_staged && fin) {
+        fin = ptx::mbar_wait(c.bar_acc, 0, c.lim_ns, c.abort_flag, p.err, 22);
+        fin = __all_sync(0xffffffffu, fin);
     }
-    fin = softmax_bar_and(fin && ok);
+    softmax_bar_sync<NT>();  // the exchange slots are free again
+    if (ok) {
+        xch[(0 * TPR + h) * 128 + row] = l[0];
+        xch[(1 * TPR + h) * 128 + row] = l[1];
+    }
+    fin = softmax_bar_and<NT>(fin && ok);
     if (!fin)
         return;
     ptx::tc_fence_after();
 #pragma unroll 1
     for (int t = 0; t < 2; ++t) {
-        const float lt = l[t] + xch[(t * 2 + (h ^ 1)) * 128 + row];
+        float lt = l[t];
+#pragma unroll
+        for (int o = 1; o < TPR; ++o)
+            lt += xch[(t * TPR + ((h + o) % TPR)) * 128 + row];
         const uint32_t tO = c.tmem + lane_addr + c.col_o[t];
         const int64_t rg = q0 + t * 128 + row;  // row inside the pair
         const int64_t orow = (int64_t)bh * pr.out_T + pr.out_t0 + rg + row_off;
@@ -208,7 +254,7 @@ __device__ __forceinline__ void softmax_warps(const SoftmaxCtx &c, const BlockPa
         const bool merging = pr.mode != kStore;
         bool use_acc = false;  // an accumulator row with lse = -inf is empty: not read
         if (merging && valid) {
-            const float a = pr.lse[orow];
+            const float a = lse_run[t];
             use_acc = a > -INFINITY;
             const float M = fmaxf(a, lse_b);
             if (M > -INFINITY) {
@@ -224,14 +270,13 @@ __device__ __forceinline__ void softmax_warps(const SoftmaxCtx &c, const BlockPa
                 wb = 0.f;
             }
         }
-        softmax_bar_sync();  // both halves have read the running lse
         if (valid && h == 0)
             pr.lse[orow] = lse_out;
 #pragma unroll 1
-        for (int k = 0; k < D / 64; ++k) {
-            const int col = h * (D / 2) + k * 32;  // first output column of this chunk
+        for (int k = 0; k < OC / 32; ++k) {
+            const int col = h * OC + k * 32;  // first output column of this chunk
             uint32_t o[32];
-            if (n > 0) {
+            if ((t == 0 ? n0 : n) > 0) {  // a tile with no key step has no O
                 ptx::tmem_ld32(tO + col, o);
                 ptx::tmem_ld_wait(o);
             } else {
@@ -243,9 +288,11 @@ __device__ __forceinline__ void softmax_warps(const SoftmaxCtx &c, const BlockPa
                 float v[32];
                 if (use_acc) {
                     const float4 *src = reinterpret_cast<const float4 *>(pr.acc + orow * D + col);
+                    // staged: row `row` of box col/32, 16-byte piece i at i ^ (row & 7)
+                    const uint32_t line = c.acc_smem[t] + (uint32_t)(col / 32) * c.acc_box_bytes + (uint32_t)row * 128u;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float4 x = src[i];
+                        const float4 x = c.acc_staged ? ld_shared_v4(line + ((uint32_t)(i ^ (row & 7)) << 4)) : src[i];
                         v[4 * i] = fmaf(u2f(o[4 * i]), wb, x.x * wa);
                         v[4 * i + 1] = fmaf(u2f(o[4 * i + 1]), wb, x.y * wa);
                         v[4 * i + 2] = fmaf(u2f(o[4 * i + 2]), wb, x.z * wa);

@@ -166,9 +166,9 @@ rsa_status rsa_merge_finalize(const float *o_acc, const float *lse_acc, const vo
 
 /*
  * Bytes of device workspace rsa_ring_attn_fwd needs for this shape (written
- * to *bytes): an fp32 accumulator [B, H, T, d] (none when N = 1) plus room
- * for one round's partial results (fp32 o and lse of every pair in the
- * largest round).
+ * to *bytes): an fp32 accumulator [B, H, T, d] (none when N = 1).  (The
+ * RSA_RING_SEPARATE_MERGE variant needs more; see
+ * rsa_ring_attn_workspace_size_ex.)
  */
 rsa_status rsa_ring_attn_workspace_size(rsa_dtype dt, int B, int H, int64_t T, int d, int N,
                                         int causal, size_t *bytes);
@@ -179,9 +179,11 @@ rsa_status rsa_ring_attn_workspace_size(rsa_dtype dt, int B, int H, int64_t T, i
  * round r pairs query chunk i with KV chunk (i - r) mod N; when causal, pairs
  * whose KV chunk lies after the query chunk are skipped, leaving N(N+1)/2
  * pairs.  Round 0 (the diagonal) writes straight into the accumulator (or into
- * out/lse for a chunk visited once); every later round computes its pairs'
- * partials and merges them; a chunk's last merge writes out (dtype dt) and
- * lse.  Requires N >= 1 and N dividing T.  `workspace` must hold
+ * out/lse for a chunk visited once); in every later round each pair's block
+ * epilogue folds its (o, lse) into the fp32 accumulator with the merge rule of
+ * rsa_merge, and a chunk's last pair writes out (dtype dt) and lse.  (Pairs of
+ * one round never share a query chunk, so the in-place fold is race-free.)
+ * Requires N >= 1 and N dividing T.  `workspace` must hold
  * rsa_ring_attn_workspace_size() bytes.  The call only enqueues kernels on
  * `stream` (no synchronisation, no allocation), so a stream capture records
  * the whole ring as one CUDA graph that can be replayed.
@@ -232,14 +234,21 @@ rsa_status rsa_ring_attn_fwd_timed(const void *q, const void *k, const void *v, 
 /*
  * Ring variant flags for rsa_ring_attn_fwd_ex / rsa_ring_attn_workspace_size_ex.
  *
- * RSA_RING_FUSED_MERGE: rounds after the first do not write partials; each
- * pair's block epilogue folds its (o, lse) straight into the fp32 accumulator
- * with the same merge rule as rsa_merge (and the chunk's last pair writes
- * out/lse).  No merge launches and no partial buffers: the workspace is the
- * accumulator alone.  Pairs of one round never share a query chunk, so the
- * in-place fold is race-free.
+ * RSA_RING_FUSED_MERGE (the default of rsa_ring_attn_fwd; 0 means the same):
+ * rounds after the first do not write partials; each pair's block epilogue
+ * folds its (o, lse) straight into the fp32 accumulator with the same merge
+ * rule as rsa_merge (and the chunk's last pair writes out/lse).  No merge
+ * launches and no partial buffers: the workspace is the accumulator alone.
+ *
+ * RSA_RING_SEPARATE_MERGE: every round after the first writes its pairs'
+ * fp32 partials (o, lse) to the workspace and one merge-kernel launch folds
+ * them into the accumulator (the chunk's last merge writes out/lse).  The
+ * workspace adds one round's partials.  Same results within rounding.
+ *
+ * The two exclude each other.
  */
 #define RSA_RING_FUSED_MERGE 1u
+#define RSA_RING_SEPARATE_MERGE 2u
 
 /* Workspace bytes for rsa_ring_attn_fwd_ex with these flags. */
 rsa_status rsa_ring_attn_workspace_size_ex(rsa_dtype dt, int B, int H, int64_t T, int d, int N,
@@ -250,7 +259,8 @@ rsa_status rsa_ring_attn_workspace_size_ex(rsa_dtype dt, int B, int H, int64_t T
  * ev_start, ev_stop and kind are all non-NULL it records events around each
  * launch as rsa_ring_attn_fwd_timed does (kind 0 block attention, 1 merge);
  * when all three are NULL nothing is recorded.  *n_launches (if non-NULL)
- * receives the number of kernel launches.  flags = 0 is rsa_ring_attn_fwd.
+ * receives the number of kernel launches.  flags = 0 (or
+ * RSA_RING_FUSED_MERGE) is rsa_ring_attn_fwd.
  */
 rsa_status rsa_ring_attn_fwd_ex(const void *q, const void *k, const void *v, rsa_dtype dt,
                                 int B, int H, int64_t T, int d, int N, int causal, unsigned flags,

@@ -19,7 +19,7 @@ def test_gpu_arm_prints_one_full_contract_line():
     B, H, T, d, N = 1, 4, 2048, 128, 4
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--shape", f"{B},{H},{T},{d},{N},1",
                         "--steps", "3", "--warmup", "3", "--e2e-steps", "2", "--cpu-budget-s", "2",
-                        "--no-fused", "--no-decode", "--no-two-pass", "--no-other-workloads",
+                        "--no-separate-merge", "--no-decode", "--no-two-pass", "--no-other-workloads",
                         "--h2d-settle-s", "0"],
                        cwd=ROOT, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stderr[-3000:]

@@ -106,7 +106,8 @@ def test_ring_is_deterministic():
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def test_ring_outputs_leave_guard_bytes_alone():
+@pytest.mark.parametrize("fused", [True, False], ids=["fused_merge", "merge_kernel"])
+def test_ring_outputs_leave_guard_bytes_alone(fused):
     need_cuda()
     B, H, T, d, N = 1, 2, 1000, 128, 8
     (q, k, v), (qd, kd, vd) = qkv_cuda(B, H, T, d, torch.bfloat16, seed=8)
@@ -114,11 +115,11 @@ def test_ring_outputs_leave_guard_bytes_alone():
     n_o = B * H * T * d
     o_buf = torch.full((pad + n_o + pad,), 3.0, dtype=torch.bfloat16, device="cuda")
     l_buf = torch.full((pad + B * H * T + pad,), 3.0, dtype=torch.float32, device="cuda")
-    need = rsa.workspace_size(torch.bfloat16, B, H, T, d, N, True)
+    need = rsa.workspace_size(torch.bfloat16, B, H, T, d, N, True, fused=fused)
     ws_buf = torch.full((pad + need + pad,), 0x5a, dtype=torch.uint8, device="cuda")
     out = o_buf[pad:pad + n_o].view(B, H, T, d)
     lse = l_buf[pad:pad + B * H * T].view(B, H, T)
-    rsa.ring_attn(qd, kd, vd, N, True, out=out, lse=lse, workspace=ws_buf[pad:pad + need])
+    rsa.ring_attn(qd, kd, vd, N, True, out=out, lse=lse, workspace=ws_buf[pad:pad + need], fused=fused)
     torch.cuda.synchronize()
     assert torch.all(o_buf[:pad] == 3) and torch.all(o_buf[pad + n_o:] == 3)
     assert torch.all(l_buf[:pad] == 3) and torch.all(l_buf[pad + B * H * T:] == 3)
@@ -131,13 +132,14 @@ def test_timed_ring_records_every_launch():
     need_cuda()
     B, H, T, d, N = 1, 2, 1024, 128, 4
     (q, k, v), (qd, kd, vd) = qkv_cuda(B, H, T, d, torch.bfloat16, seed=9)
-    n = rsa.ring_launch_count(N, True)
+    n = rsa.ring_launch_count(N, True, fused=False)
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
     out = torch.empty_like(qd)
     lse = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
-    ws = torch.empty(rsa.workspace_size(torch.bfloat16, B, H, T, d, N, True), dtype=torch.uint8, device="cuda")
-    kinds = rsa.ring_attn_timed(qd, kd, vd, N, True, out, lse, ws, ev0, ev1)
+    ws = torch.empty(rsa.workspace_size(torch.bfloat16, B, H, T, d, N, True, fused=False), dtype=torch.uint8,
+                     device="cuda")
+    kinds = rsa.ring_attn_timed(qd, kd, vd, N, True, out, lse, ws, ev0, ev1, fused=False)
     torch.cuda.synchronize()
     assert kinds == [0] + [0, 1] * (N - 1)
     assert all(a.elapsed_time(b) >= 0 for a, b in zip(ev0, ev1))

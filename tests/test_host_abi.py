@@ -58,25 +58,33 @@ def test_schedule_causal_needs_and_counts():
 
 
 def test_launch_count():
+    # default (merge folded into the block epilogue): one block launch per round
     assert rsa.ring_launch_count(1, True) == 1
-    assert rsa.ring_launch_count(4, True) == 1 + 2 * 3
-    assert rsa.ring_launch_count(16, True) == 1 + 2 * 15
-    assert rsa.ring_launch_count(4, False) == 1 + 2 * 3
+    assert rsa.ring_launch_count(4, True) == 4
+    assert rsa.ring_launch_count(16, True) == 16
+    # separate merge kernel: a block and a merge launch per round after the first
+    assert rsa.ring_launch_count(4, True, fused=False) == 1 + 2 * 3
+    assert rsa.ring_launch_count(16, True, fused=False) == 1 + 2 * 15
+    assert rsa.ring_launch_count(4, False, fused=False) == 1 + 2 * 3
 
 
 def test_workspace_size():
     import torch
     B, H, T, d, N = 8, 64, 32768, 128, 4
-    ws = rsa.workspace_size(torch.bfloat16, B, H, T, d, N, True)
+    ws = rsa.workspace_size(torch.bfloat16, B, H, T, d, N, True, fused=False)
     acc = B * H * T * d * 4
     Tc = T // N
     blk = (N - 1) * B * H * Tc * d * 4 + (N - 1) * B * H * Tc * 4  # fp32 partials
     assert ws == acc + blk
     assert rsa.workspace_size(torch.bfloat16, 1, 1, 256, 128, 1, True) == 0
-    assert rsa.workspace_size(torch.bfloat16, B, H, T, d, N, True, fused=True) == acc
-    assert rsa.ring_launch_count(4, True, fused=True) == 4
+    assert rsa.workspace_size(torch.bfloat16, B, H, T, d, N, True) == acc  # the default: the accumulator alone
+    lib = rsa.load()
+    n = ctypes.c_size_t(0)
+    assert lib.rsa_ring_attn_workspace_size(1, B, H, T, d, N, 1, ctypes.byref(n)) == 0 and n.value == acc
+    assert lib.rsa_ring_attn_workspace_size_ex(1, B, H, T, d, N, 1, 3, ctypes.byref(n)) == 1  # both flags
+    assert lib.rsa_ring_attn_workspace_size_ex(1, B, H, T, d, N, 1, 4, ctypes.byref(n)) == 1  # unknown flag
     # non-causal rounds have N pairs
-    ws2 = rsa.workspace_size(torch.float32, 1, 1, 256, 64, 4, False)
+    ws2 = rsa.workspace_size(torch.float32, 1, 1, 256, 64, 4, False, fused=False)
     assert ws2 == 256 * 64 * 4 + 4 * 64 * 64 * 4 + 4 * 64 * 4
 
 
