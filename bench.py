@@ -533,9 +533,13 @@ def main():
         del probe
         torch.cuda.empty_cache()
         # which host pages are huge right before the timed loop (copies from
-        # base-page parts of a block have run far slower)
-        host_before = {name: rsa.host_info(t) for name, t in
+        # base-page parts of a block have run far slower), and one more warm-up
+        # call with the copy paths as they now stand (the first pass of the
+        # copy kernel over host memory has been slow)
+        host_before = {name: dict(rsa.host_info(t), path=rsa.host_copy_path(t)) for name, t in
                        (("q", qh), ("k", kh), ("v", vh), ("out+lse", bufs["out_host"]))}
+        rsa.ring_attn_from_host(qh, kh, vh, N, causal, device=dev, buffers=bufs)
+        torch.cuda.synchronize()
         e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
         barrier()
         torch.cuda.synchronize()
@@ -559,7 +563,7 @@ def main():
                "h2d_settle": {"probes_gbs": settle, "waited_s": round(settle_s, 1),
                               "target_gbs": args.h2d_settle_gbs, "limit_s": args.h2d_settle_s},
                "host_buffers": host_before,
-               "host_buffers_after": {name: rsa.host_info(t) for name, t in
+               "host_buffers_after": {name: dict(rsa.host_info(t), path=rsa.host_copy_path(t)) for name, t in
                                       (("q", qh), ("k", kh), ("v", vh), ("out+lse", bufs["out_host"]))},
                "slabs": rsa.slab_plan(B * H),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}

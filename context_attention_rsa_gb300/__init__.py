@@ -26,7 +26,7 @@ __all__ = [
     "RsaError", "load", "library_path", "block_attn_fwd", "merge", "merge_finalize",
     "ring_attn", "ring_attn_noalloc", "ring_attn_timed", "decode_attn", "decode_workspace_size",
     "two_pass_attn", "two_pass_workspace_size", "ring_attn_from_host", "slab_plan", "host_empty", "host_kind",
-    "host_info", "host_workspace_size",
+    "host_info", "host_workspace_size", "set_host_copy_mode", "host_copy_path",
     "workspace_size", "ring_schedule", "set_block_kernel",
     "set_wait_limit_ns", "check_device_error", "selftest_wait_timeout", "version",
     "RSA_F32", "RSA_BF16",
@@ -90,6 +90,8 @@ _SIGS = {
     "rsa_host_info": [_c_void_p, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t),
                       ctypes.POINTER(_i32)],
     "rsa_host_slab_plan": [_i32, _i32, _i32, ctypes.POINTER(_i32), _i32, ctypes.POINTER(_i32)],
+    "rsa_set_host_copy_mode": [_i32],
+    "rsa_host_copy_path": [_c_void_p, ctypes.c_size_t, ctypes.POINTER(_i32)],
     "rsa_ring_attn_host_workspace_size": [_i32, _i32, _i32, _i64, _i32, _i32, _i32,
                                           ctypes.POINTER(ctypes.c_size_t)],
     "rsa_ring_attn_fwd_host": [_c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _i64, _i32, _i32, _i32,
@@ -325,7 +327,9 @@ def ring_attn_timed(q, k, v, N: int, causal: bool, out, lse, workspace, events_s
 
 
 def ring_launch_count(N: int, causal: bool, fused: bool = True) -> int:
-    """Kernel launches one ring makes (block-attention plus merge launches)."""
+    """Kernel launches one ring makes: one block-attention launch per round
+    (up to 32 pairs each), plus, with fused=False, one merge launch per round
+    after the first."""
     n = 0
     for r in range(N):
         np_ = len(ring_schedule(N, causal, r))
@@ -394,6 +398,24 @@ def host_kind(t: torch.Tensor) -> str:
     if ours:
         return host_info(t)["kind"]
     return "pinned" if t.is_pinned() else "pageable"
+
+
+HOST_COPY_MODES = {"auto": 0, "engines": 1, "sm": 2}
+
+
+def set_host_copy_mode(mode: str) -> None:
+    """How ring_attn_from_host moves host tensors: "auto" (copy engines for
+    library blocks still on huge pages and for pageable memory, a copy kernel
+    for other page-locked memory), "engines" or "sm"."""
+    _call("rsa_set_host_copy_mode", HOST_COPY_MODES[mode])
+
+
+def host_copy_path(t: torch.Tensor) -> str:
+    """"engines" or "kernel": how ring_attn_from_host would move this host
+    tensor now."""
+    path = ctypes.c_int(0)
+    _call("rsa_host_copy_path", t.data_ptr(), t.numel() * t.element_size(), ctypes.byref(path))
+    return "engines" if path.value == 1 else "kernel"
 
 
 def slab_plan(BH: int, groups: int = 8, ramp: bool = True) -> List[int]:

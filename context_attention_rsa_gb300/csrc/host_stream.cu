@@ -20,11 +20,18 @@
 // measured to lose most of their copy-engine bandwidth after the memory sat
 // idle for some seconds on this machine class (211 GB/s falling towards
 // 10-20 GB/s), while page-locked memory on transparent huge pages kept its
-// speed.  rsa_host_alloc therefore hands out huge-page-backed memory,
-// registered with the driver.
+// speed -- as long as the kernel kept those pages huge, which it does not
+// always do.  rsa_host_alloc therefore hands out huge-page-backed memory,
+// registered with the driver, and each call picks how to move each tensor:
+// the copy engines for a block that is still on huge pages (they run beside
+// the ring almost for free), otherwise a copy kernel whose SM loads and
+// stores reach the page-locked memory through its mapped address (measured
+// at full link speed from such memory, at the price of slowing the ring by
+// about a tenth while both run).
 #include <sys/mman.h>
 #include <unistd.h>
 
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <map>
@@ -55,6 +62,8 @@ struct HostBlock {
     size_t bytes;     // usable bytes at the block's address
     int kind;         // RSA_HOST_HUGE or RSA_HOST_PINNED
 };
+
+std::atomic<int> g_copy_mode{RSA_HOST_COPY_AUTO};
 
 std::mutex g_host_mu;
 std::map<uintptr_t, HostBlock> g_host_blocks;
@@ -123,6 +132,109 @@ void touch(void *p, size_t len)
         });
     for (auto &th : pool)
         th.join();
+}
+
+// ---------------------------------------------------------------------------
+// Moving a slab: copy engines or a copy kernel
+// ---------------------------------------------------------------------------
+
+// 16-byte units from src to dst, one of them page-locked host memory reached
+// through its mapped address.  One CTA per SM, 256 threads of 32 registers:
+// it fits beside a block-attention CTA, which leaves that much free.
+constexpr int kCopyThreads = 256;
+
+__global__ void __launch_bounds__(kCopyThreads)
+    slab_copy_kernel(uint4 *__restrict__ dst, const uint4 *__restrict__ src, size_t n16)
+{
+    size_t i = (size_t)blockIdx.x * kCopyThreads + threadIdx.x;
+    const size_t stride = (size_t)gridDim.x * kCopyThreads;
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+        const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
+        dst[i] = a;
+        dst[i + stride] = b;
+        dst[i + 2 * stride] = c;
+        dst[i + 3 * stride] = d;
+    }
+    for (; i < n16; i += stride)
+        dst[i] = src[i];
+}
+
+// How one host tensor of a call moves (RSA_HOST_PATH_*), and, for the copy
+// kernel, its mapped device address.
+struct HostPath {
+    int path = RSA_HOST_PATH_ENGINES;
+    char *mapped = nullptr;
+};
+
+// The library block containing [p, p + bytes), if any.
+bool find_block(const void *p, size_t bytes, uintptr_t *start, HostBlock *hb)
+{
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    auto it = g_host_blocks.upper_bound(a);
+    if (it == g_host_blocks.begin())
+        return false;
+    --it;
+    if (a < it->first || a + bytes > it->first + it->second.bytes)
+        return false;
+    *start = it->first;
+    *hb = it->second;
+    return true;
+}
+
+rsa_status choose_path(const void *p, size_t bytes, int mode, HostPath *hp)
+{
+    hp->path = RSA_HOST_PATH_ENGINES;
+    hp->mapped = nullptr;
+    cudaPointerAttributes attr{};
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // pageable memory on older runtimes
+        return RSA_OK;
+    }
+    if (attr.type != cudaMemoryTypeHost || !attr.devicePointer)
+        return RSA_OK;  // pageable: the runtime stages the copy
+    const char *mapped = static_cast<const char *>(attr.devicePointer);
+    bool kernel = mode == RSA_HOST_COPY_SM;
+    if (mode == RSA_HOST_COPY_AUTO) {
+        uintptr_t start = 0;
+        HostBlock hb{};
+        // the copy engines while the block is still (90%) on huge pages
+        kernel = !(find_block(p, bytes, &start, &hb) && hb.kind == RSA_HOST_HUGE &&
+                   smaps_huge_bytes(reinterpret_cast<void *>(start)) >= hb.bytes / 10 * 9);
+    }
+    if (kernel && (reinterpret_cast<uintptr_t>(mapped) & 15u) == 0) {
+        hp->path = RSA_HOST_PATH_KERNEL;
+        hp->mapped = const_cast<char *>(mapped);
+    }
+    return RSA_OK;
+}
+
+// Copy `bytes` (a multiple of 16) between device memory and host memory at
+// host offset `off`, by the tensor's path, on stream s.
+rsa_status move(const HostPath &hp, void *dev, const void *host_src, void *host_dst, size_t off, size_t bytes,
+                bool to_device, int n_sm, cudaStream_t s)
+{
+    if (hp.path == RSA_HOST_PATH_KERNEL && (bytes & 15u) == 0 && (reinterpret_cast<uintptr_t>(dev) & 15u) == 0 &&
+        (off & 15u) == 0) {
+        char *h = hp.mapped + off;
+        if (to_device)
+            slab_copy_kernel<<<n_sm, kCopyThreads, 0, s>>>(static_cast<uint4 *>(dev), reinterpret_cast<const uint4 *>(h),
+                                                          bytes / 16);
+        else
+            slab_copy_kernel<<<n_sm, kCopyThreads, 0, s>>>(reinterpret_cast<uint4 *>(h),
+                                                          static_cast<const uint4 *>(dev), bytes / 16);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return fail(RSA_ERR_CUDA, "copy kernel launch: %s", cudaGetErrorString(e));
+        return RSA_OK;
+    }
+    cudaError_t e = to_device ? cudaMemcpyAsync(dev, static_cast<const char *>(host_src) + off, bytes,
+                                                cudaMemcpyHostToDevice, s)
+                              : cudaMemcpyAsync(static_cast<char *>(host_dst) + off, dev, bytes, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess)
+        return fail(RSA_ERR_CUDA, "cudaMemcpyAsync: %s", cudaGetErrorString(e));
+    return RSA_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -340,6 +452,26 @@ rsa_status rsa_host_info(const void *ptr, size_t *bytes, size_t *huge_bytes, int
     return RSA_OK;
 }
 
+rsa_status rsa_set_host_copy_mode(int mode)
+{
+    if (mode < RSA_HOST_COPY_AUTO || mode > RSA_HOST_COPY_SM)
+        return fail(RSA_ERR_INVALID_ARG, "host copy mode %d is not 0, 1 or 2", mode);
+    g_copy_mode.store(mode);
+    return RSA_OK;
+}
+
+rsa_status rsa_host_copy_path(const void *ptr, size_t bytes, int *path)
+{
+    if (!ptr || !path)
+        return fail(RSA_ERR_INVALID_ARG, "ptr and path must not be NULL");
+    HostPath hp;
+    rsa_status st = choose_path(ptr, bytes, g_copy_mode.load(), &hp);
+    if (st != RSA_OK)
+        return st;
+    *path = hp.path;
+    return RSA_OK;
+}
+
 rsa_status rsa_host_slab_plan(int BH, int groups, int ramp, int *slabs, int cap, int *n_slabs)
 {
     if (BH < 1 || groups < 1 || !n_slabs)
@@ -415,6 +547,15 @@ rsa_status rsa_ring_attn_fwd_host(const void *q_host, const void *k_host, const 
 
     const size_t esz = dt == RSA_BF16 ? 2 : 4;
     const size_t head_bytes = (size_t)T * (size_t)d * esz;
+    const size_t total_bytes = (size_t)BH * head_bytes;
+    int n_sm = 0;
+    TRY(cuda_ok(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute"));
+    const int mode = g_copy_mode.load();
+    HostPath hp[5];
+    const void *host_ptr[5] = {q_host, k_host, v_host, out_host, lse_host};
+    const size_t host_bytes[5] = {total_bytes, total_bytes, total_bytes, total_bytes, (size_t)BH * (size_t)T * 4};
+    for (int i = 0; i < 5; ++i)
+        TRY(choose_path(host_ptr[i], host_bytes[i], mode, &hp[i]));
     char *wsb = static_cast<char *>(workspace);
     char *slot_base[2] = {wsb, wsb + 4 * w.in_bytes + w.lse_bytes};
     void *ring_ws = wsb + 2 * (4 * w.in_bytes + w.lse_bytes);
@@ -439,8 +580,7 @@ rsa_status rsa_ring_attn_fwd_host(const void *q_host, const void *k_host, const 
             TRY(cuda_ok(cudaStreamWaitEvent(ds.s_in, ev_comp[g - 2], 0), "cudaStreamWaitEvent"));
         char *dst[3] = {dq, dk, dv};
         for (int t = 0; t < 3; ++t)
-            TRY(cuda_ok(cudaMemcpyAsync(dst[t], src[t] + off, nbytes, cudaMemcpyHostToDevice, ds.s_in),
-                        "cudaMemcpyAsync (host to device)"));
+            TRY(move(hp[t], dst[t], src[t], nullptr, off, nbytes, true, n_sm, ds.s_in));
         TRY(cuda_ok(cudaEventRecord(ev_in[g], ds.s_in), "cudaEventRecord"));
         // ring on the caller's stream (slot reuse: slab g-2's outputs are out)
         TRY(cuda_ok(cudaStreamWaitEvent(main, ev_in[g], 0), "cudaStreamWaitEvent"));
@@ -450,12 +590,9 @@ rsa_status rsa_ring_attn_fwd_host(const void *q_host, const void *k_host, const 
         TRY(cuda_ok(cudaEventRecord(ev_comp[g], main), "cudaEventRecord"));
         // copy out
         TRY(cuda_ok(cudaStreamWaitEvent(ds.s_out, ev_comp[g], 0), "cudaStreamWaitEvent"));
-        TRY(cuda_ok(cudaMemcpyAsync(static_cast<char *>(out_host) + off, dout, nbytes, cudaMemcpyDeviceToHost,
-                                    ds.s_out),
-                    "cudaMemcpyAsync (device to host)"));
-        TRY(cuda_ok(cudaMemcpyAsync(lse_host + (size_t)h0 * (size_t)T, dlse, (size_t)n * (size_t)T * 4,
-                                    cudaMemcpyDeviceToHost, ds.s_out),
-                    "cudaMemcpyAsync (device to host)"));
+        TRY(move(hp[3], dout, nullptr, out_host, off, nbytes, false, n_sm, ds.s_out));
+        TRY(move(hp[4], dlse, nullptr, lse_host, (size_t)h0 * (size_t)T * 4, (size_t)n * (size_t)T * 4, false, n_sm,
+                 ds.s_out));
         TRY(cuda_ok(cudaEventRecord(ev_out[g], ds.s_out), "cudaEventRecord"));
         h0 += n;
     }

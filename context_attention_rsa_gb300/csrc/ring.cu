@@ -9,13 +9,13 @@
 // running-statistics rescale ("But softmax seems to require all attention
 // scores at once").
 //
-// Each round's partials are kept in fp32 in the workspace: a bf16 partial
-// would add a second rounding on top of the final bf16 output.
-//
 // Here every chunk is resident on the one GPU, so "sending a KV block to the
 // next GPU" becomes pointing the next round's pairs at another chunk's base
 // offset: no copy, no collective.  One block-attention launch covers all pairs
-// of a round and one merge launch folds them in.
+// of a round.  By default its epilogue folds each pair into the fp32
+// accumulator; with RSA_RING_SEPARATE_MERGE the round's partials go to the
+// workspace in fp32 (a bf16 partial would add a second rounding on top of the
+// final bf16 output) and one merge launch folds them in.
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>

@@ -296,6 +296,38 @@ rsa_status rsa_host_free(void *ptr);
 rsa_status rsa_host_info(const void *ptr, size_t *bytes, size_t *huge_bytes, int *kind);
 
 /*
+ * How rsa_ring_attn_fwd_host moves each host tensor (process wide; set
+ * before the calls it should affect):
+ *   RSA_HOST_COPY_AUTO     (default) per tensor and per call: the copy
+ *                          engines (cudaMemcpyAsync) for a block from
+ *                          rsa_host_alloc that is still at least 90% on huge
+ *                          pages, and for pageable memory; a copy kernel
+ *                          otherwise, i.e. for page-locked memory on base
+ *                          pages (cudaHostAlloc, cudaHostRegister, or a
+ *                          library block the kernel has split)
+ *   RSA_HOST_COPY_ENGINES  always the copy engines
+ *   RSA_HOST_COPY_SM       the copy kernel for all page-locked memory
+ * The copy kernel (one CTA of 256 threads per SM, beside the ring's CTAs)
+ * reads and writes the page-locked memory through its mapped address.
+ * Measured on GB300 hosts: copy-engine transfers of page-locked memory on
+ * 64 KiB pages fell from 211 GB/s towards 10 GB/s within seconds of idling,
+ * and huge-page blocks copied at 5-120 GB/s once the kernel had split some
+ * of their pages, while the copy kernel moved the same memory at 193-211
+ * GB/s alone and about 127 GB/s beside the ring, which it slowed by about a
+ * tenth; copy engines beside the ring slowed it by 2%.
+ * Returns RSA_ERR_INVALID_ARG for another mode.
+ */
+enum { RSA_HOST_COPY_AUTO = 0, RSA_HOST_COPY_ENGINES = 1, RSA_HOST_COPY_SM = 2 };
+rsa_status rsa_set_host_copy_mode(int mode);
+
+/*
+ * The path rsa_ring_attn_fwd_host would take now for the host buffer
+ * [ptr, ptr + bytes): RSA_HOST_PATH_ENGINES or RSA_HOST_PATH_KERNEL.
+ */
+enum { RSA_HOST_PATH_ENGINES = 1, RSA_HOST_PATH_KERNEL = 2 };
+rsa_status rsa_host_copy_path(const void *ptr, size_t bytes, int *path);
+
+/*
  * The slab plan of rsa_ring_attn_fwd_host: how many heads each slab holds, in
  * streaming order, for BH = B*H heads cut into about `groups` slabs of at most
  * ceil(BH/groups) heads.  With ramp, the plan starts at an eighth of the
@@ -323,7 +355,8 @@ rsa_status rsa_ring_attn_host_workspace_size(rsa_dtype dt, int B, int H, int64_t
  * into slabs (rsa_host_slab_plan(B*H, 8, 1)): while the ring of slab g runs on
  * `stream`, slab g+1 is copied in and slab g-1 copied out on two copy streams
  * the library creates for the current device on its first call there (with
- * their events; all are kept until the process exits).  Device slabs are
+ * their events; all are kept until the process exits).  Each tensor moves
+ * by the copy engines or by a copy kernel (rsa_set_host_copy_mode).  Device slabs are
  * double-buffered in `workspace` (a DEVICE pointer, 256-byte aligned, at
  * least rsa_ring_attn_host_workspace_size() bytes).  The results equal
  * rsa_ring_attn_fwd's bit for bit.

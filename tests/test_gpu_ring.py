@@ -198,24 +198,35 @@ def test_fused_and_unfused_rings_agree_and_fused_launches_only_block_kernels():
     assert torch.equal(out[:, :, :T // N], o_a[:, :, :T // N])  # chunk 0 is never merged
 
 
+@pytest.mark.parametrize("mode", ["auto", "engines", "sm"])
 @pytest.mark.parametrize("B,H,T,N,dtype", [(2, 5, 1024, 4, torch.bfloat16), (1, 64, 512, 4, torch.bfloat16),
-                                             (2, 37, 384, 3, torch.bfloat16), (1, 3, 256, 4, torch.float32)])
-def test_ring_from_host_matches_device_ring(B, H, T, N, dtype):
+                                             (2, 37, 384, 3, torch.bfloat16), (1, 3, 256, 4, torch.float32),
+                                             (1, 6, 130, 2, torch.bfloat16)])
+def test_ring_from_host_matches_device_ring(B, H, T, N, dtype, mode):
     # rsa_ring_attn_fwd_host (head slabs streamed through the GPU, copies on
     # the library's streams) gives exactly the device ring's result: every
     # head is its own problem.  64 and 74 heads run ramped plans of slabs of
     # 1 to 7 and 1 to 5 heads; torch-pinned inputs are accepted as well.
     need_cuda()
+    # The copy path of each tensor follows the mode: torch-pinned inputs move
+    # by the copy kernel in "auto" and "sm", by the copy engines in "engines";
+    # rows of 130 x 4 bytes of lse are not 16-byte multiples and fall back to
+    # the copy engines.
     d = 64 if dtype == torch.float32 else 128
     q, k, v = (t.pin_memory() for t in qkv_cuda(B, H, T, d, dtype, seed=13)[0])
     ref_o, ref_l = rsa.ring_attn(q.cuda(), k.cuda(), v.cuda(), N, True)
-    bufs = {}
-    for _ in range(2):  # second call reuses the buffers
-        oh, lh, bufs = rsa.ring_attn_from_host(q, k, v, N, True, buffers=bufs)
-        torch.cuda.synchronize()
-        assert torch.equal(oh, ref_o.cpu()) and torch.equal(lh, ref_l.cpu())
-        oh.fill_(float("nan"))
-        lh.fill_(float("nan"))
+    rsa.set_host_copy_mode(mode)
+    try:
+        assert rsa.host_copy_path(q) == ("engines" if mode == "engines" else "kernel")
+        bufs = {}
+        for _ in range(2):  # second call reuses the buffers
+            oh, lh, bufs = rsa.ring_attn_from_host(q, k, v, N, True, buffers=bufs)
+            torch.cuda.synchronize()
+            assert torch.equal(oh, ref_o.cpu()) and torch.equal(lh, ref_l.cpu())
+            oh.fill_(float("nan"))
+            lh.fill_(float("nan"))
+    finally:
+        rsa.set_host_copy_mode("auto")
 
 
 def test_host_empty_is_page_locked_huge_and_streams_bit_exactly():
@@ -232,6 +243,10 @@ def test_host_empty_is_page_locked_huge_and_streams_bit_exactly():
             assert info["huge_bytes"] >= info["bytes"] * 9 // 10
         assert rsa.host_kind(th) == info["kind"]
     ref_o, ref_l = rsa.ring_attn(q.cuda(), k.cuda(), v.cuda(), N, True)
+    for th in (qh, kh, vh):  # "auto": copy engines while the block is on huge pages
+        info = rsa.host_info(th)
+        huge = info["kind"] == "registered-huge" and info["huge_bytes"] >= info["bytes"] * 9 // 10
+        assert rsa.host_copy_path(th) == ("engines" if huge else "kernel")
     bufs = {}
     oh, lh, bufs = rsa.ring_attn_from_host(qh, kh, vh, N, True, buffers=bufs)
     torch.cuda.synchronize()

@@ -230,3 +230,12 @@ def test_host_alloc_rejects_bad_arguments():
     cnt = ctypes.c_int(0)
     assert lib.rsa_host_slab_plan(512, 8, 1, slabs, 4, ctypes.byref(cnt)) == 1 and cnt.value == 14
     assert lib.rsa_host_slab_plan(0, 8, 1, slabs, 4, ctypes.byref(cnt)) == 1
+
+
+def test_host_copy_mode_setter():
+    lib = rsa.load()
+    assert lib.rsa_set_host_copy_mode(3) == 1 and lib.rsa_set_host_copy_mode(-1) == 1
+    for mode in (1, 2, 0):
+        assert lib.rsa_set_host_copy_mode(mode) == 0
+    path = ctypes.c_int(0)
+    assert lib.rsa_host_copy_path(None, 16, ctypes.byref(path)) == 1
