@@ -28,6 +28,8 @@
 // stores reach the page-locked memory through its mapped address (measured
 // at full link speed from such memory, at the price of slowing the ring by
 // about a tenth while both run).
+#include <fcntl.h>
+#include <sys/ioctl.h>
 #include <sys/mman.h>
 #include <unistd.h>
 
@@ -79,7 +81,11 @@ size_t read_size_file(const char *path, size_t fallback)
     return (n == 1 && v > 0) ? (size_t)v : fallback;
 }
 
-size_t huge_page_bytes() { return read_size_file("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", 2u << 20); }
+size_t huge_page_bytes()
+{
+    static const size_t h = read_size_file("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", 2u << 20);
+    return h;
+}
 
 // AnonHugePages of the mapping that starts exactly at `start` (the guards
 // keep the block's mapping from merging with its neighbours); 0 if unknown.
@@ -108,6 +114,96 @@ size_t smaps_huge_bytes(const void *start)
     }
     fclose(f);
     return huge;
+}
+
+// The kernel's page-table scan of one address range (the PAGEMAP_SCAN ioctl
+// of /proc/self/pagemap, Linux 6.7 on), declared here so that older headers
+// build.  Its cost grows with the range scanned, where a read of
+// /proc/self/smaps walks every mapping of the process (tens of milliseconds
+// in a process holding some GB of base pages).  Regions whose pages are
+// mapped as huge pages carry kScanHuge.
+struct ScanRegion {
+    uint64_t start, end, categories;
+};
+struct ScanArg {
+    uint64_t size, flags, start, end, walk_end, vec, vec_len, max_pages;
+    uint64_t category_inverted, category_mask, category_anyof_mask, return_mask;
+};
+constexpr uint64_t kScanHuge = 1u << 6;
+const unsigned long kPagemapScan = _IOWR('f', 16, ScanArg);
+
+// Bytes of [lo, hi) mapped by huge pages, through the pagemap descriptor fd;
+// -1 if the kernel cannot say.
+long long scan_huge(int fd, uintptr_t lo, uintptr_t hi)
+{
+    ScanRegion reg[32];
+    long long huge = 0;
+    while (lo < hi) {
+        ScanArg a{};
+        a.size = sizeof a;
+        a.start = lo;
+        a.end = hi;
+        a.vec = reinterpret_cast<uint64_t>(reg);
+        a.vec_len = sizeof reg / sizeof reg[0];
+        a.category_mask = kScanHuge;
+        a.return_mask = kScanHuge;
+        const int n = ioctl(fd, kPagemapScan, &a);
+        if (n < 0)
+            return -1;
+        for (int i = 0; i < n; ++i)
+            huge += (long long)(reg[i].end - reg[i].start);
+        if (a.walk_end <= lo)
+            break;
+        lo = a.walk_end;
+    }
+    return huge;
+}
+
+// Share (0..1) of [p, p + len) on huge pages; -1 if the kernel cannot say.
+// Exact, or with `sample` set and the range longer than kWindows huge pages,
+// estimated from kWindows huge-page windows spread evenly over it (what a
+// per-call decision needs, at a cost that does not grow with the range).
+// /proc/self/pagemap is opened per call: a descriptor kept open would go on
+// describing the parent after a fork.
+double huge_share(const void *p, size_t len, bool sample)
+{
+    if (len == 0)
+        return 1.0;
+    const int fd = open("/proc/self/pagemap", O_RDONLY | O_CLOEXEC);
+    if (fd < 0)
+        return -1.0;
+    constexpr size_t kWindows = 64;
+    const size_t H = huge_page_bytes();
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p), hi = lo + len;
+    const uintptr_t a0 = (lo + H - 1) / H * H, a1 = hi / H * H;
+    const size_t n_win = a1 > a0 ? (a1 - a0) / H : 0;
+    double share = -1.0;
+    if (!sample || n_win <= kWindows) {
+        const long long h = scan_huge(fd, lo, hi);
+        if (h >= 0)
+            share = (double)h / (double)len;
+    } else {
+        long long h = 0;
+        for (size_t i = 0; i < kWindows && h >= 0; ++i) {
+            const uintptr_t w = a0 + (i * n_win / kWindows) * H;
+            const long long hw = scan_huge(fd, w, w + H);
+            h = hw < 0 ? -1 : h + hw;
+        }
+        if (h >= 0)
+            share = (double)h / (double)(kWindows * H);
+    }
+    close(fd);
+    return share;
+}
+
+// Huge-page bytes of a library block: the range scan where the kernel has
+// it, else the AnonHugePages of its mapping.
+size_t block_huge_bytes(const void *blk, size_t bytes)
+{
+    const double share = huge_share(blk, bytes, false);
+    if (share >= 0.0)
+        return (size_t)(share * (double)bytes + 0.5);
+    return smaps_huge_bytes(blk);
 }
 
 // Zero the block with a few threads so that every page exists (and is a huge
@@ -199,9 +295,15 @@ rsa_status choose_path(const void *p, size_t bytes, int mode, HostPath *hp)
     if (mode == RSA_HOST_COPY_AUTO) {
         uintptr_t start = 0;
         HostBlock hb{};
-        // the copy engines while the block is still (90%) on huge pages
-        kernel = !(find_block(p, bytes, &start, &hb) && hb.kind == RSA_HOST_HUGE &&
-                   smaps_huge_bytes(reinterpret_cast<void *>(start)) >= hb.bytes / 10 * 9);
+        // the copy engines while the tensor's pages are still (90%) huge
+        if (find_block(p, bytes, &start, &hb) && hb.kind == RSA_HOST_HUGE) {
+            double share = huge_share(p, bytes, true);
+            if (share < 0.0)  // no range scan: the whole block's count
+                share = (double)smaps_huge_bytes(reinterpret_cast<void *>(start)) / (double)hb.bytes;
+            kernel = share < 0.9;
+        } else {
+            kernel = true;
+        }
     }
     if (kernel && (reinterpret_cast<uintptr_t>(mapped) & 15u) == 0) {
         hp->path = RSA_HOST_PATH_KERNEL;
@@ -377,7 +479,7 @@ rsa_status rsa_host_alloc(size_t bytes, void **ptr)
             munmap(base, map_len);
             break;
         }
-        const size_t h = smaps_huge_bytes(blk);
+        const size_t h = block_huge_bytes(blk, len);
         if (!best_blk || h > best_huge) {
             if (best_blk) {
                 cudaHostUnregister(best_blk);
@@ -448,7 +550,7 @@ rsa_status rsa_host_info(const void *ptr, size_t *bytes, size_t *huge_bytes, int
     if (kind)
         *kind = hb.kind;
     if (huge_bytes)
-        *huge_bytes = hb.kind == RSA_HOST_HUGE ? smaps_huge_bytes(ptr) : 0;
+        *huge_bytes = hb.kind == RSA_HOST_HUGE ? block_huge_bytes(ptr, hb.bytes) : 0;
     return RSA_OK;
 }
 

@@ -299,12 +299,17 @@ rsa_status rsa_host_info(const void *ptr, size_t *bytes, size_t *huge_bytes, int
  * How rsa_ring_attn_fwd_host moves each host tensor (process wide; set
  * before the calls it should affect):
  *   RSA_HOST_COPY_AUTO     (default) per tensor and per call: the copy
- *                          engines (cudaMemcpyAsync) for a block from
- *                          rsa_host_alloc that is still at least 90% on huge
- *                          pages, and for pageable memory; a copy kernel
+ *                          engines (cudaMemcpyAsync) for a tensor in a block
+ *                          from rsa_host_alloc whose pages are still at least
+ *                          90% huge, and for pageable memory; a copy kernel
  *                          otherwise, i.e. for page-locked memory on base
  *                          pages (cudaHostAlloc, cudaHostRegister, or a
- *                          library block the kernel has split)
+ *                          library block the kernel has split).  The share
+ *                          is read from the kernel's page tables over 64
+ *                          huge-page windows spread over the tensor
+ *                          (Linux 6.7 on; older kernels: the block's
+ *                          AnonHugePages in /proc/self/smaps, which costs
+ *                          milliseconds per call in a large process)
  *   RSA_HOST_COPY_ENGINES  always the copy engines
  *   RSA_HOST_COPY_SM       the copy kernel for all page-locked memory
  * The copy kernel (one CTA of 256 threads per SM, beside the ring's CTAs)

@@ -229,6 +229,19 @@ def test_ring_from_host_matches_device_ring(B, H, T, N, dtype, mode):
         rsa.set_host_copy_mode("auto")
 
 
+def test_ring_from_host_accepts_pageable_tensors():
+    # Pageable host memory moves through the runtime's staged copies (the
+    # copy engines); the result is still the device ring's, bit for bit.
+    need_cuda()
+    B, H, T, d, N = 1, 8, 1024, 128, 4
+    (q, k, v), _ = qkv_cuda(B, H, T, d, torch.bfloat16, seed=17)
+    assert not q.is_pinned() and rsa.host_copy_path(q) == "engines"
+    ref_o, ref_l = rsa.ring_attn(q.cuda(), k.cuda(), v.cuda(), N, True)
+    oh, lh, _ = rsa.ring_attn_from_host(q, k, v, N, True)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, ref_o.cpu()) and torch.equal(lh, ref_l.cpu())
+
+
 def test_host_empty_is_page_locked_huge_and_streams_bit_exactly():
     need_cuda()
     B, H, T, d, N = 1, 64, 512, 128, 4
