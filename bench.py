@@ -510,9 +510,19 @@ def main():
         del q, k, v, out, lse, ws
         torch.cuda.empty_cache()
         bufs = {}
-        for _ in range(2):  # warm-up: the library's copy streams, the workspace, the host outputs
+        warm_ms = []
+
+        def timed_warmup():
+            w0 = torch.cuda.Event(enable_timing=True)
+            w1 = torch.cuda.Event(enable_timing=True)
+            w0.record(stream)
             rsa.ring_attn_from_host(qh, kh, vh, N, causal, device=dev, buffers=bufs)
-        torch.cuda.synchronize()
+            w1.record(stream)
+            torch.cuda.synchronize()
+            warm_ms.append(round(w0.elapsed_time(w1), 2))
+
+        for _ in range(2):  # warm-up: the library's copy streams, the workspace, the host outputs
+            timed_warmup()
         # Host-to-device bandwidth just before the timed loop: one copy of Q's
         # host buffer.  Such copies have run far below their usual ~211 GB/s on
         # some boxes; the probe is repeated every 5 s, for at most
@@ -536,13 +546,13 @@ def main():
         del probe
         torch.cuda.empty_cache()
         # which host pages are huge right before the timed loop (copies from
-        # base-page parts of a block have run far slower), and one more warm-up
-        # call with the copy paths as they now stand (the first pass of the
-        # copy kernel over host memory has been slow)
+        # base-page parts of a block have run far slower), and two more
+        # warm-up calls with the copy paths as they now stand (on some hosts
+        # the first call after the probes above ran 2-3x slower than the rest)
         host_before = {name: dict(rsa.host_info(t), path=rsa.host_copy_path(t)) for name, t in
                        (("q", qh), ("k", kh), ("v", vh), ("out+lse", bufs["out_host"]))}
-        rsa.ring_attn_from_host(qh, kh, vh, N, causal, device=dev, buffers=bufs)
-        torch.cuda.synchronize()
+        timed_warmup()
+        timed_warmup()
         e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
         barrier()
         torch.cuda.synchronize()
@@ -561,7 +571,7 @@ def main():
         d2h = bufs["out_host"].numel() * bufs["out_host"].element_size() + bufs["lse_host"].numel() * 4
         e2e = {"value": whole_job_tflops(flops, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "call": "rsa_ring_attn_fwd_host", "steps": args.e2e_steps,
-               "step_ms": [round(x, 2) for x in e_steps], "clocks": e_clk,
+               "step_ms": [round(x, 2) for x in e_steps], "warmup_ms": warm_ms, "clocks": e_clk,
                "h2d_gbs_before": round(h2d_probe, 1),
                "h2d_settle": {"probes_gbs": settle, "waited_s": round(settle_s, 1),
                               "target_gbs": args.h2d_settle_gbs, "limit_s": args.h2d_settle_s},
