@@ -132,12 +132,24 @@ struct ScanArg {
 constexpr uint64_t kScanHuge = 1u << 6;
 const unsigned long kPagemapScan = _IOWR('f', 16, ScanArg);
 
-// Bytes of [lo, hi) mapped by huge pages, through the pagemap descriptor fd;
-// -1 if the kernel cannot say.
-long long scan_huge(int fd, uintptr_t lo, uintptr_t hi)
+using Regions = std::vector<std::pair<uintptr_t, uintptr_t>>;
+
+// The regions of [lo, hi) mapped by huge pages, in address order (adjacent
+// huge pages come back as one region); false if the kernel cannot say.
+// /proc/self/pagemap is opened per call: a descriptor kept open would go on
+// describing the parent after a fork.  The cost grows with the page-table
+// entries walked: a few for a range on huge pages, one per base page where
+// the kernel has split them.
+bool huge_regions(const void *p, size_t len, Regions *out)
 {
+    out->clear();
+    const int fd = open("/proc/self/pagemap", O_RDONLY | O_CLOEXEC);
+    if (fd < 0)
+        return false;
     ScanRegion reg[32];
-    long long huge = 0;
+    uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    const uintptr_t hi = lo + len;
+    bool ok = true;
     while (lo < hi) {
         ScanArg a{};
         a.size = sizeof a;
@@ -148,61 +160,44 @@ long long scan_huge(int fd, uintptr_t lo, uintptr_t hi)
         a.category_mask = kScanHuge;
         a.return_mask = kScanHuge;
         const int n = ioctl(fd, kPagemapScan, &a);
-        if (n < 0)
-            return -1;
-        for (int i = 0; i < n; ++i)
-            huge += (long long)(reg[i].end - reg[i].start);
+        if (n < 0) {
+            ok = false;
+            break;
+        }
+        for (int i = 0; i < n; ++i) {
+            if (!out->empty() && out->back().second == reg[i].start)
+                out->back().second = reg[i].end;
+            else
+                out->emplace_back(reg[i].start, reg[i].end);
+        }
         if (a.walk_end <= lo)
             break;
         lo = a.walk_end;
     }
-    return huge;
+    close(fd);
+    return ok;
 }
 
-// Share (0..1) of [p, p + len) on huge pages; -1 if the kernel cannot say.
-// Exact, or with `sample` set and the range longer than kWindows huge pages,
-// estimated from kWindows huge-page windows spread evenly over it (what a
-// per-call decision needs, at a cost that does not grow with the range).
-// /proc/self/pagemap is opened per call: a descriptor kept open would go on
-// describing the parent after a fork.
-double huge_share(const void *p, size_t len, bool sample)
+// Bytes of [lo, lo + len) inside the regions.
+size_t bytes_in(const Regions &r, uintptr_t lo, size_t len)
 {
-    if (len == 0)
-        return 1.0;
-    const int fd = open("/proc/self/pagemap", O_RDONLY | O_CLOEXEC);
-    if (fd < 0)
-        return -1.0;
-    constexpr size_t kWindows = 64;
-    const size_t H = huge_page_bytes();
-    const uintptr_t lo = reinterpret_cast<uintptr_t>(p), hi = lo + len;
-    const uintptr_t a0 = (lo + H - 1) / H * H, a1 = hi / H * H;
-    const size_t n_win = a1 > a0 ? (a1 - a0) / H : 0;
-    double share = -1.0;
-    if (!sample || n_win <= kWindows) {
-        const long long h = scan_huge(fd, lo, hi);
-        if (h >= 0)
-            share = (double)h / (double)len;
-    } else {
-        long long h = 0;
-        for (size_t i = 0; i < kWindows && h >= 0; ++i) {
-            const uintptr_t w = a0 + (i * n_win / kWindows) * H;
-            const long long hw = scan_huge(fd, w, w + H);
-            h = hw < 0 ? -1 : h + hw;
-        }
-        if (h >= 0)
-            share = (double)h / (double)(kWindows * H);
+    const uintptr_t hi = lo + len;
+    size_t b = 0;
+    for (const auto &x : r) {
+        const uintptr_t a = x.first > lo ? x.first : lo, e = x.second < hi ? x.second : hi;
+        if (e > a)
+            b += e - a;
     }
-    close(fd);
-    return share;
+    return b;
 }
 
 // Huge-page bytes of a library block: the range scan where the kernel has
 // it, else the AnonHugePages of its mapping.
 size_t block_huge_bytes(const void *blk, size_t bytes)
 {
-    const double share = huge_share(blk, bytes, false);
-    if (share >= 0.0)
-        return (size_t)(share * (double)bytes + 0.5);
+    Regions r;
+    if (huge_regions(blk, bytes, &r))
+        return bytes_in(r, reinterpret_cast<uintptr_t>(blk), bytes);
     return smaps_huge_bytes(blk);
 }
 
@@ -255,12 +250,20 @@ __global__ void __launch_bounds__(kCopyThreads)
         dst[i] = src[i];
 }
 
-// How one host tensor of a call moves (RSA_HOST_PATH_*), and, for the copy
-// kernel, its mapped device address.
+// How one host tensor of a call moves.  In automatic mode a tensor in a
+// library block is decided copy by copy: its huge-page regions are read once
+// per call, and each copy goes by the copy engines while its own range lies
+// (90%) on huge pages, else by the copy kernel -- a block the kernel has
+// split in a few places then moves mostly by the engines.
 struct HostPath {
-    int path = RSA_HOST_PATH_ENGINES;
-    char *mapped = nullptr;
+    int path = RSA_HOST_PATH_ENGINES;  // the tensor as a whole
+    char *mapped = nullptr;            // mapped device address (page-locked memory)
+    uintptr_t host = 0;                // the tensor's host address
+    bool per_copy = false;             // decide each copy from `huge`
+    Regions huge;                      // the tensor's huge-page regions (per_copy)
 };
+
+constexpr double kHugeShare = 0.9;  // engines at or above this huge-page share
 
 // The library block containing [p, p + bytes), if any.
 bool find_block(const void *p, size_t bytes, uintptr_t *start, HostBlock *hb)
@@ -282,6 +285,9 @@ rsa_status choose_path(const void *p, size_t bytes, int mode, HostPath *hp)
 {
     hp->path = RSA_HOST_PATH_ENGINES;
     hp->mapped = nullptr;
+    hp->host = reinterpret_cast<uintptr_t>(p);
+    hp->per_copy = false;
+    hp->huge.clear();
     cudaPointerAttributes attr{};
     cudaError_t e = cudaPointerGetAttributes(&attr, p);
     if (e != cudaSuccess) {
@@ -291,25 +297,34 @@ rsa_status choose_path(const void *p, size_t bytes, int mode, HostPath *hp)
     if (attr.type != cudaMemoryTypeHost || !attr.devicePointer)
         return RSA_OK;  // pageable: the runtime stages the copy
     const char *mapped = static_cast<const char *>(attr.devicePointer);
+    if ((reinterpret_cast<uintptr_t>(mapped) & 15u) != 0)
+        return RSA_OK;  // the copy kernel moves 16-byte units
+    hp->mapped = const_cast<char *>(mapped);
     bool kernel = mode == RSA_HOST_COPY_SM;
     if (mode == RSA_HOST_COPY_AUTO) {
         uintptr_t start = 0;
         HostBlock hb{};
-        // the copy engines while the tensor's pages are still (90%) huge
+        kernel = true;  // page-locked memory on base pages
         if (find_block(p, bytes, &start, &hb) && hb.kind == RSA_HOST_HUGE) {
-            double share = huge_share(p, bytes, true);
-            if (share < 0.0)  // no range scan: the whole block's count
-                share = (double)smaps_huge_bytes(reinterpret_cast<void *>(start)) / (double)hb.bytes;
-            kernel = share < 0.9;
-        } else {
-            kernel = true;
+            if (huge_regions(p, bytes, &hp->huge)) {
+                hp->per_copy = true;
+                kernel = (double)bytes_in(hp->huge, hp->host, bytes) < kHugeShare * (double)bytes;
+            } else {  // no range scan: the whole block's count
+                kernel = (double)smaps_huge_bytes(reinterpret_cast<void *>(start)) < kHugeShare * (double)hb.bytes;
+            }
         }
     }
-    if (kernel && (reinterpret_cast<uintptr_t>(mapped) & 15u) == 0) {
-        hp->path = RSA_HOST_PATH_KERNEL;
-        hp->mapped = const_cast<char *>(mapped);
-    }
+    hp->path = kernel ? RSA_HOST_PATH_KERNEL : RSA_HOST_PATH_ENGINES;
     return RSA_OK;
+}
+
+// The path of one copy of `bytes` at offset `off` into the tensor.
+int copy_path(const HostPath &hp, size_t off, size_t bytes)
+{
+    if (!hp.per_copy || !hp.mapped)
+        return hp.path;
+    const bool huge = (double)bytes_in(hp.huge, hp.host + off, bytes) >= kHugeShare * (double)bytes;
+    return huge ? RSA_HOST_PATH_ENGINES : RSA_HOST_PATH_KERNEL;
 }
 
 // Copy `bytes` (a multiple of 16) between device memory and host memory at
@@ -317,8 +332,8 @@ rsa_status choose_path(const void *p, size_t bytes, int mode, HostPath *hp)
 rsa_status move(const HostPath &hp, void *dev, const void *host_src, void *host_dst, size_t off, size_t bytes,
                 bool to_device, int n_sm, cudaStream_t s)
 {
-    if (hp.path == RSA_HOST_PATH_KERNEL && (bytes & 15u) == 0 && (reinterpret_cast<uintptr_t>(dev) & 15u) == 0 &&
-        (off & 15u) == 0) {
+    if (copy_path(hp, off, bytes) == RSA_HOST_PATH_KERNEL && hp.mapped && (bytes & 15u) == 0 &&
+        (reinterpret_cast<uintptr_t>(dev) & 15u) == 0 && (off & 15u) == 0) {
         char *h = hp.mapped + off;
         if (to_device)
             slab_copy_kernel<<<n_sm, kCopyThreads, 0, s>>>(static_cast<uint4 *>(dev), reinterpret_cast<const uint4 *>(h),

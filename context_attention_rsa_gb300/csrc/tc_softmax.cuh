@@ -17,10 +17,10 @@
 // halves of a row agree on the row max through shared memory behind a named
 // barrier and keep their own part of the row sum l.
 //
-// Each thread stores its 64 P values as two 16-column pieces (the first
-// store overlaps the arithmetic of the second piece), waits for both, and
-// calls arrive(t): once every softmax thread has arrived, P_t and the
-// rescaled O_t are complete in TMEM for the PV MMA.
+// Each thread packs its P values into bf16 pairs and writes them with one
+// TMEM store (32 packed columns for 64 keys), waits for it, and calls
+// arrive(t): once every softmax thread has arrived, P_t and the rescaled O_t
+// are complete in TMEM for the PV MMA.
 // The kept maximum m only moves when the new one exceeds it by more than 8
 // (log2 units); o, l and lse all use the same m, so the result is exact up
 // to rounding whatever m is kept.

@@ -298,18 +298,18 @@ rsa_status rsa_host_info(const void *ptr, size_t *bytes, size_t *huge_bytes, int
 /*
  * How rsa_ring_attn_fwd_host moves each host tensor (process wide; set
  * before the calls it should affect):
- *   RSA_HOST_COPY_AUTO     (default) per tensor and per call: the copy
- *                          engines (cudaMemcpyAsync) for a tensor in a block
- *                          from rsa_host_alloc whose pages are still at least
- *                          90% huge, and for pageable memory; a copy kernel
- *                          otherwise, i.e. for page-locked memory on base
- *                          pages (cudaHostAlloc, cudaHostRegister, or a
- *                          library block the kernel has split).  The share
- *                          is read from the kernel's page tables over 64
- *                          huge-page windows spread over the tensor
- *                          (Linux 6.7 on; older kernels: the block's
- *                          AnonHugePages in /proc/self/smaps, which costs
- *                          milliseconds per call in a large process)
+ *   RSA_HOST_COPY_AUTO     (default) per copy: the copy engines
+ *                          (cudaMemcpyAsync) for pageable memory and for a
+ *                          copy whose range of a block from rsa_host_alloc
+ *                          is still at least 90% on huge pages; a copy
+ *                          kernel otherwise, i.e. for page-locked memory on
+ *                          base pages (cudaHostAlloc, cudaHostRegister) and
+ *                          for the parts of a library block that the kernel
+ *                          has split.  Each call reads each such tensor's
+ *                          huge-page regions from the kernel's page tables
+ *                          once (Linux 6.7 on); older kernels give no
+ *                          regions, and then the whole tensor goes one way,
+ *                          by its block's AnonHugePages in /proc/self/smaps
  *   RSA_HOST_COPY_ENGINES  always the copy engines
  *   RSA_HOST_COPY_SM       the copy kernel for all page-locked memory
  * The copy kernel (one CTA of 256 threads per SM, beside the ring's CTAs)
@@ -326,8 +326,10 @@ enum { RSA_HOST_COPY_AUTO = 0, RSA_HOST_COPY_ENGINES = 1, RSA_HOST_COPY_SM = 2 }
 rsa_status rsa_set_host_copy_mode(int mode);
 
 /*
- * The path rsa_ring_attn_fwd_host would take now for the host buffer
- * [ptr, ptr + bytes): RSA_HOST_PATH_ENGINES or RSA_HOST_PATH_KERNEL.
+ * The path rsa_ring_attn_fwd_host would take now for one copy of the host
+ * buffer [ptr, ptr + bytes): RSA_HOST_PATH_ENGINES or RSA_HOST_PATH_KERNEL.
+ * The call itself copies a tensor slab by slab and decides each copy on its
+ * own range, so a tensor whose block is split in places moves partly each way.
  */
 enum { RSA_HOST_PATH_ENGINES = 1, RSA_HOST_PATH_KERNEL = 2 };
 rsa_status rsa_host_copy_path(const void *ptr, size_t bytes, int *path);

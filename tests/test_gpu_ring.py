@@ -274,6 +274,57 @@ def test_host_empty_is_page_locked_huge_and_streams_bit_exactly():
     assert addr not in rsa._host_blocks
 
 
+def _huge_page_bytes():
+    try:
+        with open("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size") as f:
+            return int(f.read())
+    except OSError:
+        return 0
+
+
+def test_ring_from_host_splits_copies_by_huge_page_regions():
+    # A block the kernel has split in one place moves by the copy engines
+    # where it is still huge and by the copy kernel where it is not, and the
+    # call's results stay bit-exact.  The split is made here the way the
+    # kernel makes one: changing the protection of one base page inside a
+    # huge page (and changing it back) remaps that huge page with base pages.
+    need_cuda()
+    import ctypes
+    import os
+    hp = _huge_page_bytes()
+    page = os.sysconf("SC_PAGE_SIZE")
+    if hp <= 0 or hp > (512 << 20):
+        pytest.skip("no transparent huge pages of a usable size")
+    T, d, N = 8192, 128, 4
+    H = 2 * hp // (T * d * 2)  # each tensor spans two huge pages
+    g = torch.Generator(device="cuda").manual_seed(61)
+    q, k, v = (torch.randn((1, H, T, d), generator=g, device="cuda").to(torch.bfloat16) for _ in range(3))
+    qh, kh, vh = (rsa.host_empty(t.shape, t.dtype) for t in (q, k, v))
+    for th, t in ((qh, q), (kh, k), (vh, v)):
+        th.copy_(t)
+    info = rsa.host_info(kh)
+    if info["kind"] != "registered-huge" or info["huge_bytes"] < 2 * hp:
+        pytest.skip("the host block did not get huge pages")
+    torch.cuda.synchronize()
+    libc = ctypes.CDLL(None, use_errno=True)
+    libc.mprotect.argtypes = (ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int)
+    at = kh.data_ptr() + hp + hp // 2  # inside the second huge page
+    assert libc.mprotect(at, page, 1) == 0  # PROT_READ
+    assert libc.mprotect(at, page, 3) == 0  # PROT_READ | PROT_WRITE
+    after = rsa.host_info(kh)
+    if after["huge_bytes"] > info["huge_bytes"] - hp:
+        pytest.skip("the kernel kept the huge page mapped whole")
+    flat = kh.view(-1)
+    half = hp // 2 // 2  # bf16 elements in half a huge page
+    assert rsa.host_copy_path(flat[:half]) == "engines"  # inside the first, intact huge page
+    assert rsa.host_copy_path(flat[2 * half:3 * half]) == "kernel"  # inside the split one
+    assert rsa.host_copy_path(kh) == "kernel"  # half of the tensor is on base pages
+    ref_o, ref_l = rsa.ring_attn(q, k, v, N, True)
+    oh, lh, _ = rsa.ring_attn_from_host(qh, kh, vh, N, True)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, ref_o.cpu()) and torch.equal(lh, ref_l.cpu())
+
+
 def test_ring_from_host_waits_for_the_callers_stream():
     # The copies start only after work already enqueued on the caller's
     # stream: inputs written there just before the call are the ones used.
