@@ -247,9 +247,9 @@ def main():
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip timing the ring on the ragged and million-token workloads")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
-    ap.add_argument("--h2d-settle-gbs", type=float, default=150.0,
-                    help="before the e2e timed loop, wait for a host-to-device probe this fast")
-    ap.add_argument("--h2d-settle-s", type=float, default=90.0, help="longest wait for that probe")
+    ap.add_argument("--e2e-settle-tol", type=float, default=0.1,
+                    help="before the e2e timed loop, warm up until two calls in a row agree this closely")
+    ap.add_argument("--e2e-settle-s", type=float, default=30.0, help="longest such warm-up")
     ap.add_argument("--shape", default=None,
                     help="B,H,T,d,N,causal: a bf16 normal-recipe workload instead of --workload (profiling)")
     args = ap.parse_args()
@@ -523,36 +523,33 @@ def main():
 
         for _ in range(2):  # warm-up: the library's copy streams, the workspace, the host outputs
             timed_warmup()
-        # Host-to-device bandwidth just before the timed loop: one copy of Q's
-        # host buffer.  Such copies have run far below their usual ~211 GB/s on
-        # some boxes; the probe is repeated every 5 s, for at most
-        # --h2d-settle-s seconds, until it reaches --h2d-settle-gbs.  Every
-        # probe and the time waited go into the output line.
+        # Host-to-device bandwidth of one copy-engine copy of Q's host buffer,
+        # for the record (the call itself routes split parts of a block to the
+        # copy kernel, so this probe can be far slower than the call).
         probe = torch.empty_like(qh, device=dev)
-        settle, t_settle = [], time.time()
-        while True:
-            p0 = torch.cuda.Event(enable_timing=True)
-            p1 = torch.cuda.Event(enable_timing=True)
-            p0.record(stream)
-            probe.copy_(qh, non_blocking=True)
-            p1.record(stream)
-            torch.cuda.synchronize()
-            h2d_probe = qh.numel() * qh.element_size() / (p0.elapsed_time(p1) * 1e-3) / 1e9
-            settle.append(round(h2d_probe, 1))
-            if h2d_probe >= args.h2d_settle_gbs or time.time() - t_settle >= args.h2d_settle_s:
-                break
-            time.sleep(5.0)
-        settle_s = time.time() - t_settle
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        probe.copy_(qh, non_blocking=True)
+        p1.record(stream)
+        torch.cuda.synchronize()
+        h2d_probe = qh.numel() * qh.element_size() / (p0.elapsed_time(p1) * 1e-3) / 1e9
         del probe
         torch.cuda.empty_cache()
-        # which host pages are huge right before the timed loop (copies from
-        # base-page parts of a block have run far slower), and two more
-        # warm-up calls with the copy paths as they now stand (on some hosts
-        # the first call after the probes above ran 2-3x slower than the rest)
+        # Which host pages are huge right before the timed loop, then warm-up
+        # calls until two in a row agree within --e2e-settle-tol (at most
+        # --e2e-settle-s seconds): on some hosts calls ran 2-15x slower for a
+        # while (one host's second call took 1454 ms, later ones 97 ms).
         host_before = {name: dict(rsa.host_info(t), path=rsa.host_copy_path(t)) for name, t in
                        (("q", qh), ("k", kh), ("v", vh), ("out+lse", bufs["out_host"]))}
+        t_settle = time.time()
         timed_warmup()
-        timed_warmup()
+        while True:
+            timed_warmup()
+            a, b = warm_ms[-2], warm_ms[-1]
+            if abs(a - b) <= args.e2e_settle_tol * min(a, b) or time.time() - t_settle >= args.e2e_settle_s:
+                break
+        settle_s = time.time() - t_settle
         e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
         barrier()
         torch.cuda.synchronize()
@@ -573,8 +570,7 @@ def main():
                "call": "rsa_ring_attn_fwd_host", "steps": args.e2e_steps,
                "step_ms": [round(x, 2) for x in e_steps], "warmup_ms": warm_ms, "clocks": e_clk,
                "h2d_gbs_before": round(h2d_probe, 1),
-               "h2d_settle": {"probes_gbs": settle, "waited_s": round(settle_s, 1),
-                              "target_gbs": args.h2d_settle_gbs, "limit_s": args.h2d_settle_s},
+               "settle": {"waited_s": round(settle_s, 1), "tol": args.e2e_settle_tol, "limit_s": args.e2e_settle_s},
                "host_buffers": host_before,
                "host_buffers_after": {name: dict(rsa.host_info(t), path=rsa.host_copy_path(t)) for name, t in
                                       (("q", qh), ("k", kh), ("v", vh), ("out+lse", bufs["out_host"]))},
