@@ -312,7 +312,8 @@ rsa_status rsa_host_info(const void *ptr, size_t *bytes, size_t *huge_bytes, int
  *                          by its block's AnonHugePages in /proc/self/smaps
  *   RSA_HOST_COPY_ENGINES  always the copy engines
  *   RSA_HOST_COPY_SM       the copy kernel for all page-locked memory
- * The copy kernel (one CTA of 256 threads per SM, beside the ring's CTAs)
+ * The copy kernel (256-thread CTAs on half as many CTAs as the GPU has SMs,
+ * beside the ring's CTAs)
  * reads and writes the page-locked memory through its mapped address.
  * Measured on GB300 hosts: copy-engine transfers of page-locked memory on
  * 64 KiB pages fell from 211 GB/s towards 10 GB/s within seconds of idling,
