@@ -365,7 +365,9 @@ __global__ void __launch_bounds__(kScoreThreads)
                     ptx::tma_store_3d(&tm_s, slot + (uint32_t)c * kChunkBytes, w.kt * 128 + 32 * c, w.qt * 128, w.bh);
                 ptx::bulk_commit_group();
             }
-            p.stats[((int64_t)w.bh * p.Tc + (int64_t)w.qt * 128 + row) * n_half + 2 * w.kt + h] = make_float2(hm, hl);
+            const int64_t si = ((int64_t)w.bh * p.Tc + (int64_t)w.qt * 128 + row) * n_half + 2 * w.kt + h;
+            if (RSA_DCHECK(si >= 0 && si < p.BH * p.Tc * n_half, p.err, 0x61, si))
+                p.stats[si] = make_float2(hm, hl);
         }
         if (threadIdx.x == 0)
             bulk_wait_group_read<0>();  // shared memory stays in use until the stores have read it
@@ -383,13 +385,16 @@ __global__ void __launch_bounds__(kScoreThreads)
 // P = e^{s-M}/L in bf16, and lse = M + ln L into the output lse.
 __global__ void __launch_bounds__(256)
     softmax_rows_kernel(const float *__restrict__ S, const float2 *__restrict__ stats, __nv_bfloat16 *__restrict__ P,
-                        float *__restrict__ lse, int64_t BH, int64_t Tc, int64_t T, int n)
+                        float *__restrict__ lse, int64_t BH, int64_t Tc, int64_t T, int n, unsigned int *err)
 {
     const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= BH * Tc)
         return;
     const int64_t n_st = T / 64;  // statistics entries of the row
+    // the row's statistics, scores and probabilities lie inside their buffers
+    if (!RSA_DCHECK(row < BH * Tc && (T & 3) == 0, err, 0x62, row))
+        return;
     const float2 *st = stats + row * n_st;
     float M = -INFINITY;
     for (int64_t i = lane; i < n_st; i += 32)
@@ -427,7 +432,9 @@ __global__ void __launch_bounds__(256)
     }
     if (lane == 0) {
         const int64_t bh = row / Tc, r = row - bh * Tc;
-        lse[bh * T + (int64_t)n * Tc + r] = empty ? -INFINITY : M + ptx::lg2(L) * 0.69314718055994531f;
+        const int64_t li = bh * T + (int64_t)n * Tc + r;
+        if (RSA_DCHECK(li >= 0 && li < BH * T, err, 0x63, li))
+            lse[li] = empty ? -INFINITY : M + ptx::lg2(L) * 0.69314718055994531f;
     }
 }
 
@@ -542,8 +549,10 @@ __global__ void __launch_bounds__(kPvThreads)
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             ptx::tc_fence_after();
-            const bool valid = (int64_t)qt * 128 + row < p.Tc;
-            __nv_bfloat16 *dst = p.out + ((int64_t)bh * p.T + (int64_t)p.n * p.Tc + (int64_t)qt * 128 + row) * D;
+            const int64_t orow = (int64_t)bh * p.T + (int64_t)p.n * p.Tc + (int64_t)qt * 128 + row;
+            const bool valid = (int64_t)qt * 128 + row < p.Tc &&
+                               RSA_DCHECK(orow >= 0 && orow < p.BH * p.T, p.err, 0x64, orow);
+            __nv_bfloat16 *dst = p.out + orow * D;
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t o[32];
@@ -633,7 +642,7 @@ cudaError_t launch_two_pass(const void *q, const void *k, const void *v, int64_t
         score_kernel<<<(unsigned)score_ctas, kScoreThreads, smem_score, s>>>(mq, mk, ms, p);
         const int64_t rows = BH * Tc;
         softmax_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
-            S, static_cast<const float2 *>(stats), static_cast<__nv_bfloat16 *>(P), lse, BH, Tc, T, n);
+            S, static_cast<const float2 *>(stats), static_cast<__nv_bfloat16 *>(P), lse, BH, Tc, T, n, err);
         pv_kernel<<<dim3((unsigned)n_qt, (unsigned)BH), kPvThreads, smem_pv, s>>>(mp, mv, p);
         e = cudaGetLastError();
         if (e != cudaSuccess)

@@ -14,7 +14,7 @@ from conftest import ROOT
 pytestmark = pytest.mark.gpu
 
 FILES = ["test_gpu_ring.py", "test_gpu_block.py", "test_gpu_decode.py", "test_gpu_block_kernels.py",
-         "test_gpu_failures.py"]
+         "test_gpu_failures.py", "test_gpu_two_pass.py", "test_gpu_fuzz.py"]
 
 
 def test_parity_cases_pass_under_the_bounds_checked_build():
