@@ -21,9 +21,14 @@
  *     (d = d_k, the head dimension); lse is [B, H, T].  "Row" means one
  *     (b, h, t) query row.
  *   - Pointers named q, k, v, out, lse, o_*, lse_* and workspace are DEVICE
- *     pointers on the current CUDA device, 16-byte aligned.  The caller owns
- *     every buffer; the library allocates no device memory and keeps no state
- *     beyond a device-side error word.
+ *     pointers on the current CUDA device, 16-byte aligned (the *_host
+ *     arguments of rsa_ring_attn_fwd_host are host pointers).  The caller
+ *     owns every buffer it passes.  The library allocates no device memory
+ *     at call time; its state is a device-side error word, the 64 MiB
+ *     scratch array of rsa_ring_attn_fwd_noalloc (reserved when its device
+ *     code loads), the host blocks handed out by rsa_host_alloc, and two
+ *     copy streams with a pool of events per device for
+ *     rsa_ring_attn_fwd_host.
  *   - Scores are scaled by 1/sqrt(d) ([P1] "Attention wants keys and values
  *     from other tokens", the attention equation); the scale is not a
  *     parameter.  lse is the natural-log log-sum-exp of the scaled scores.
@@ -363,8 +368,9 @@ rsa_status rsa_ring_attn_host_workspace_size(rsa_dtype dt, int B, int H, int64_t
  * into slabs (rsa_host_slab_plan(B*H, 8, 1)): while the ring of slab g runs on
  * `stream`, slab g+1 is copied in and slab g-1 copied out on two copy streams
  * the library creates for the current device on its first call there (with
- * their events; all are kept until the process exits).  Each tensor moves
- * by the copy engines or by a copy kernel (rsa_set_host_copy_mode).  Device slabs are
+ * their events; all are kept until the process exits).  Each slab of each
+ * tensor moves by the copy engines or by a copy kernel, decided per copy
+ * (rsa_set_host_copy_mode).  Device slabs are
  * double-buffered in `workspace` (a DEVICE pointer, 256-byte aligned, at
  * least rsa_ring_attn_host_workspace_size() bytes).  The results equal
  * rsa_ring_attn_fwd's bit for bit.
@@ -419,8 +425,9 @@ rsa_status rsa_decode_attn_fwd(const void *q, const void *k, const void *v, rsa_
  * rsa_ring_attn_fwd; the workspace holds one chunk's fp32 scores and bf16
  * probabilities, B*H*(T/N)*T*6 bytes -- the O(L/N * L) memory the online
  * merge avoids -- plus per-row statistics of each 64 keys of the row,
- * B*H*(T/N)*(T/64)*8 bytes (each part rounded up to 256 bytes).  Built for bf16 with d = 128 and T/N a multiple of 128
- * (RSA_ERR_UNSUPPORTED otherwise).
+ * B*H*(T/N)*(T/64)*8 bytes (each part rounded up to 256 bytes).  Built for
+ * bf16 with d = 128 and T/N a multiple of 128 (RSA_ERR_UNSUPPORTED
+ * otherwise).
  */
 rsa_status rsa_two_pass_workspace_size(rsa_dtype dt, int B, int H, int64_t T, int d, int N,
                                        size_t *bytes);
@@ -473,11 +480,11 @@ rsa_status rsa_debug_inject_launch_failure(int countdown);
 /*
  * 1 if this library was built with RSA_DEBUG: its kernels then check the
  * indices of their computed global-memory accesses (output, accumulator and
- * lse rows, fp32 K/V rows, merge rows); an access that fails its check is
- * skipped, and the first failure's site code and index are recorded for
- * rsa_check_device_error, which reports RSA_ERR_CUDA.  No trap.  0 for the
- * normal build, whose kernels carry no such checks.  (The two-pass kernels
- * are not covered.)
+ * lse rows, fp32 K/V rows, merge rows, the two-pass statistics, lse and
+ * output rows); an access that fails its check is skipped, and the first
+ * failure's site code and index are recorded for rsa_check_device_error,
+ * which reports RSA_ERR_CUDA.  No trap.  0 for the normal build, whose
+ * kernels carry no such checks.
  */
 int rsa_debug_checks(void);
 
