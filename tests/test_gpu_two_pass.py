@@ -60,3 +60,39 @@ def test_two_pass_rejects_unsupported_shapes():
     qf = torch.zeros(1, 1, 256, 128, dtype=torch.float32, device="cuda")
     with pytest.raises(rsa.RsaError):
         rsa.two_pass_attn(qf, qf, qf, 2, True)
+
+
+def test_two_pass_and_decode_capture_into_cuda_graphs_and_replay_bit_exactly():
+    # Both calls only enqueue kernels on the caller's stream, so a caller can
+    # capture one call and replay it (the benchmark times the two-pass form
+    # that way too); the replays must give the plain call's results exactly.
+    need_cuda()
+    B, H, T, d, N = 1, 2, 1024, 128, 4
+    (q, k, v), (qd, kd, vd) = qkv_cuda(B, H, T, d, torch.bfloat16, seed=77)
+    ref_o, ref_l = rsa.two_pass_attn(qd, kd, vd, N, True)
+    qn = qd[:, :, T - 3:].contiguous()
+    ref_do, ref_dl = rsa.decode_attn(qn, kd, vd, N, True)
+    out, lse = torch.empty_like(qd), torch.empty((B, H, T), device="cuda")
+    ws = torch.empty(rsa.two_pass_workspace_size(qd.dtype, B, H, T, d, N), dtype=torch.uint8, device="cuda")
+    dout, dlse = torch.empty_like(qn), torch.empty((B, H, 3), device="cuda")
+    dws = torch.empty(max(rsa.decode_workspace_size(qd.dtype, B, H, T, d, 3, N), 1), dtype=torch.uint8,
+                      device="cuda")
+    rsa.two_pass_attn(qd, kd, vd, N, True, out=out, lse=lse, workspace=ws)  # warm-up outside capture
+    rsa.decode_attn(qn, kd, vd, N, True, out=dout, lse=dlse, workspace=dws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            rsa.two_pass_attn(qd, kd, vd, N, True, out=out, lse=lse, workspace=ws)
+            rsa.decode_attn(qn, kd, vd, N, True, out=dout, lse=dlse, workspace=dws)
+    torch.cuda.current_stream().wait_stream(s)
+    for t in (out, lse, dout, dlse):
+        t.zero_()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    rsa.check_device_error()
+    assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
+    assert torch.equal(dout, ref_do) and torch.equal(dlse, ref_dl)
