@@ -145,3 +145,58 @@ def test_random_two_pass_matches_oracle(case):
     rsa.check_device_error()
     ro, rl = oracle.attention(q, k, v, causal)
     assert_close(out, lse, ro, rl, torch.bfloat16, what=str(case))
+
+
+def fold_cases():
+    rng = np.random.default_rng(31337)
+    out = []
+    for i in range(N_CASES // 2):
+        d = int(rng.choice([64, 128]))
+        dtype = torch.float32 if rng.random() < 0.25 else torch.bfloat16
+        T = int(rng.integers(64, 1500))
+        q_len = int(rng.integers(1, min(T, 600) + 1))
+        q_pos = int(rng.integers(0, T - q_len + 1))
+        n_pieces = int(rng.integers(1, 6))
+        cuts = sorted(set(int(x) for x in rng.integers(1, T, size=n_pieces - 1))) if n_pieces > 1 else []
+        bounds = [0] + cuts + [T]
+        pieces = [(bounds[j], bounds[j + 1] - bounds[j]) for j in range(len(bounds) - 1)]
+        order = [int(x) for x in rng.permutation(len(pieces))]
+        out.append((int(rng.integers(1, 3)), T, d, q_pos, q_len, [pieces[j] for j in order],
+                    bool(rng.random() < 0.7), dtype, int(rng.integers(0, 97)), int(rng.integers(0, 53)), 5000 + i))
+    return out
+
+
+@pytest.mark.parametrize("case", fold_cases(), ids=lambda c: "T{}d{}_q{}+{}_{}pieces_{}_{}".format(
+    c[1], c[2], c[3], c[4], len(c[5]), "causal" if c[6] else "full", _dt(c[7])))
+def test_random_fold_sequences_match_oracle(case):
+    # rsa_block_attn_fold as a rank uses it: the query block sits at row
+    # q_row0 of its own buffer, each K/V piece at row kv_row0 of a buffer of
+    # its own; the pieces (a random cut of the whole key range) are folded in
+    # a random order, FIRST .. MERGE .. LAST (ONLY for a single piece), with
+    # rows and global positions apart.
+    need_cuda()
+    from context_attention_rsa_gb300 import rank_ring as rr
+    H, T, d, q_pos, q_len, pieces, causal, dtype, q_row0, kv_row0, seed = case
+    B = 1
+    (q, k, v), _ = _qkv(B, H, T, d, dtype, seed)
+    qb = torch.full((B, H, q_row0 + q_len, d), float("nan"), dtype=dtype)
+    qb[:, :, q_row0:] = q[:, :, q_pos:q_pos + q_len]
+    qb = qb.cuda()
+    acc = torch.full((B, H, q_row0 + q_len, d), float("nan"), device="cuda")
+    lse = torch.full((B, H, q_row0 + q_len), 7.0, device="cuda")
+    out = torch.full((B, H, q_row0 + q_len, d), 3.0, dtype=dtype, device="cuda")
+    n = len(pieces)
+    for j, (kv_pos, kv_len) in enumerate(pieces):
+        fold = rr.FOLD_ONLY if n == 1 else (rr.FOLD_FIRST if j == 0 else (rr.FOLD_LAST if j == n - 1 else rr.FOLD_MERGE))
+        kb = torch.zeros((B, H, kv_row0 + kv_len, d), dtype=dtype)
+        vb = torch.zeros((B, H, kv_row0 + kv_len, d), dtype=dtype)
+        kb[:, :, kv_row0:] = k[:, :, kv_pos:kv_pos + kv_len]
+        vb[:, :, kv_row0:] = v[:, :, kv_pos:kv_pos + kv_len]
+        step = dict(q_row0=q_row0, q_pos=q_pos, q_len=q_len, kv_row0=kv_row0, kv_pos=kv_pos, kv_len=kv_len,
+                    fold=fold)
+        rr.block_attn_fold(qb, kb.cuda(), vb.cuda(), step, causal, acc if n > 1 else None, lse, out)
+        torch.cuda.synchronize()
+    rsa.check_device_error()
+    ro, rl = oracle.block(q, k, v, q_pos, q_len, 0, T, causal)
+    assert_close(out[:, :, q_row0:], lse[:, :, q_row0:], ro, rl, dtype, what=str(case[:7]))
+    assert torch.all(out[:, :, :q_row0] == 3.0) and torch.all(lse[:, :, :q_row0] == 7.0)
